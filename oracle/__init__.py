@@ -1,0 +1,152 @@
+"""fp64 CPU oracle for index-gathered attention with sinks.
+
+TEST INFRASTRUCTURE ONLY: the test suite, the package smoke check and the
+benchmark's CPU-baseline leg are the only callers. The library path never
+imports this package. The C source (`sattn_oracle.c`) shares nothing with the
+CUDA implementation.
+
+The functions take float32 numpy arrays (the exact input values, bf16 inputs
+widened) and return float64 outputs. Each accepts an optional `rows` array of
+row ids so that large workloads can be checked on sampled rows:
+  window:  row = token * H + head
+  sparse:  row = (b * M + m) * H + head
+  block:   row = i * H + head
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sattn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain C, -O2, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-std=c11", "-O2", "-fno-fast-math", "-fPIC", "-shared",
+                               "-pthread", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.oracle_window.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, P, i32,
+                                          f64, P, i64, P, P]
+            lib.oracle_sparse.argtypes = [P, P, P, i32, i32, i32, i32, i32, i32, P, i32, f64, P,
+                                          i64, P, P]
+            lib.oracle_block_sparse.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                i32, i32, i32, f64, P, i64, P, P]
+            lib.oracle_merge.argtypes = [P, P, i32, i64, i32, i32, P, P, P]
+            lib.oracle_set_threads.argtypes = [i32]
+            lib.oracle_get_threads.restype = i32
+            _lib = lib
+    return _lib
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(_load().oracle_get_threads())
+
+
+def _f32(x):
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _rows(rows):
+    if rows is None:
+        return None, 0
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    return r, int(r.size)
+
+
+def window(q, k, v, cu_seqlens, H, Hkv, d, window_left, window_right, causal, sinks,
+           sink_mode, scale, rows=None):
+    """Window attention; returns (o[nrows, d], lse[nrows]) in float64."""
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    s = None if sinks is None else _f32(sinks)
+    r, nr = _rows(rows)
+    n = nr if r is not None else int(cu[-1]) * H
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = lib.oracle_window(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), len(cu) - 1, H, Hkv, d,
+                           window_left, window_right, causal, _ptr(s), sink_mode, float(scale),
+                           _ptr(r), nr, _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_window rejected its arguments (%d)" % rc)
+    return o, lse
+
+
+def sparse(q, kv, idx, sinks, sink_mode, scale, rows=None):
+    """Gathered attention with one shared KV head; returns (o[nrows,d], lse[nrows])."""
+    lib = _load()
+    q, kv = _f32(q), _f32(kv)
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    B, M, H, d = q.shape
+    N, K = kv.shape[1], ix.shape[2]
+    s = None if sinks is None else _f32(sinks)
+    r, nr = _rows(rows)
+    n = nr if r is not None else B * M * H
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = lib.oracle_sparse(_ptr(q), _ptr(kv), _ptr(ix), B, M, H, d, N, K, _ptr(s), sink_mode,
+                           float(scale), _ptr(r), nr, _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_sparse rejected its arguments (%d)" % rc)
+    return o, lse
+
+
+def block_sparse(q, k, v, mask, q_pos0, kv_begin, kv_end, causal, scale, blk=128, rows=None):
+    """One KV chunk of block-sparse attention; returns (o_part[nrows,d], lse_part[nrows])."""
+    lib = _load()
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    M, H, d = q.shape
+    Nctx, Hkv = k.shape[0], k.shape[1]
+    r, nr = _rows(rows)
+    n = nr if r is not None else M * H
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros(n, dtype=np.float64)
+    rc = lib.oracle_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(m), M, Nctx, H, Hkv, d,
+                                 q_pos0, kv_begin, kv_end, causal, blk, float(scale), _ptr(r),
+                                 nr, _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError("oracle_block_sparse rejected its arguments (%d)" % rc)
+    return o, lse
+
+
+def merge(o_parts, lse_parts, H, sinks=None):
+    """LSE merge of C chunk partials o_parts[C,R,d], lse_parts[C,R]."""
+    lib = _load()
+    op = np.ascontiguousarray(o_parts, dtype=np.float64)
+    lp = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    C, R, d = op.shape
+    s = None if sinks is None else _f32(sinks)
+    o = np.zeros((R, d), dtype=np.float64)
+    lse = np.zeros(R, dtype=np.float64)
+    lib.oracle_merge(_ptr(op), _ptr(lp), C, R, d, H, _ptr(s), _ptr(o), _ptr(lse))
+    return o, lse
