@@ -1,0 +1,182 @@
+/*
+ * sattn: index-gathered attention forward with sinks, for GB300 (sm_103a).
+ *
+ * C ABI of libsattn.so. Every tensor argument is a DEVICE pointer to a
+ * contiguous, row-major buffer unless stated otherwise; scalars are passed by
+ * value. The caller owns every buffer; the library allocates no device or
+ * host memory and keeps no state beyond a per-device cache of attributes,
+ * tensor-map entry points and the address of its device error word.
+ *
+ * Execution: every compute call is asynchronous on `cuda_stream` (a
+ * cudaStream_t; NULL selects the per-thread default stream, never the legacy
+ * NULL stream). Calls do not synchronise unless debug mode is on.
+ *
+ * Errors: arguments are validated on the host before anything is launched and
+ * rejected with SATTN_ERR_INVALID_ARG; nothing is written in that case. A
+ * failed launch returns SATTN_ERR_CUDA. A device without sm_103 (or a
+ * combination that has no kernel) returns SATTN_ERR_UNSUPPORTED. Kernels
+ * never trap: an out-of-range index or a malformed cu_seqlens is skipped and
+ * recorded in a device error word, and every wait inside a kernel gives up
+ * after a bounded time and records a timeout. sattn_check_device() (or debug
+ * mode) reports and clears that word. No C++ exception crosses this ABI.
+ *
+ * Empty work (zero tokens, zero queries or zero rows) returns SATTN_OK and
+ * launches nothing.
+ */
+#ifndef SATTN_H_
+#define SATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SATTN_OK = 0,
+    SATTN_ERR_INVALID_ARG = 1,
+    SATTN_ERR_UNSUPPORTED = 2,
+    SATTN_ERR_CUDA = 3,
+    SATTN_ERR_DEVICE_CHECK = 4, /* a kernel skipped an out-of-range index or sequence */
+    SATTN_ERR_TIMEOUT = 5       /* a kernel-side wait gave up */
+} sattn_status;
+
+/* Sink semantics.
+ *  KEY0_BIAS  sinks[h] is added to the logit of each sequence's first key
+ *             (local position 0) wherever that key is visible; the softmax
+ *             starts empty. ("PR #49815 report", Implementation item 2 and the
+ *             `_fwd_kernel` listing: SINKS_BIAS_KEY0.) In the gathered path the
+ *             bias goes to list entries equal to 0.
+ *  NULL_LOGIT exp(sinks[h]) joins the softmax denominator only, never the
+ *             numerator (same report, the USE_SINKS default; "DeepSeek-V4
+ *             CSA/HCA walkthrough", section 4.4).
+ * `sinks` is float32[H] on the device and must be non-NULL unless NONE. */
+typedef enum {
+    SATTN_SINK_NONE = 0,
+    SATTN_SINK_KEY0_BIAS = 1,
+    SATTN_SINK_NULL_LOGIT = 2
+} sattn_sink_mode;
+
+/* Element type of q/k/v/kv/o. Accumulation is always fp32. */
+typedef enum { SATTN_F32 = 0, SATTN_BF16 = 1 } sattn_dtype;
+
+/* Key-block size of the block-sparse mask. */
+#define SATTN_BLOCK 128
+
+/*
+ * Sliding-window attention over packed varlen sequences
+ * ("PR #49815 report", `_forward_window_attn` and `context_attention_fwd`
+ * call: cu_seqlens, sliding_window_q/k = w, is_causal = False, per-head sinks).
+ *
+ *   q [T, H, d], k/v [T, Hkv, d], o [T, H, d]   (dtype), T = total_tokens
+ *   lse [T, H] float32 natural-log denominator of each row, or NULL
+ *   cu_seqlens int32 [num_seqs + 1] on the device, cu_seqlens[0] = 0,
+ *     non-decreasing, cu_seqlens[num_seqs] = T
+ *   max_seqlen >= every sequence length (used to size the grid)
+ *
+ * Query i sees key j iff both are in the same sequence and, with local
+ * positions, -window_left <= j - i <= window_right (a negative bound means
+ * unbounded on that side) and, if causal, j <= i. Query head h reads KV head
+ * h / (H / Hkv). Logits are scale * <q, k>. o has q's dtype (round to
+ * nearest even for bf16). With dtype BF16 and d = 128 the tcgen05 kernel
+ * runs; other combinations run the SIMT kernel.
+ * Requirements: H % Hkv == 0, d in {64, 128}, num_seqs >= 0.
+ */
+sattn_status sattn_window_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                              int32_t max_seqlen, int32_t H, int32_t Hkv, int32_t d,
+                              int32_t window_left, int32_t window_right, int32_t causal,
+                              const float *sinks, sattn_sink_mode sink_mode, float scale,
+                              sattn_dtype dtype, void *cuda_stream);
+
+/*
+ * Gathered attention over a [window ring | compressed] cache with one KV head
+ * shared by all query heads ("DeepSeek-V4 CSA/HCA walkthrough", section 2.3
+ * step 7 `sparse_attn(q, kv_cache, topk_idxs, attn_sink, scale)`, sections
+ * 3.3 and 4.1-4.4).
+ *
+ *   q [B, M, H, d], kv_cache [B, N, d] (each row is both key and value),
+ *   topk_idxs int32 [B, M, K] with entries in [-1, N); -1 is an invalid entry
+ *     and contributes nothing; other entries count with multiplicity.
+ *   o [B, M, H, d] (dtype), lse [B, M, H] float32 or NULL.
+ *   workspace: NULL or a caller-owned device buffer of at least
+ *     sattn_sparse_workspace_bytes(B, M, H, d, K) bytes, 256-byte aligned.
+ *     With a workspace the index list may be split across CTAs and the
+ *     partial results merged through their LSE on the device; without one
+ *     each query's list is processed by a single CTA.
+ * Requirements: d == 128 for BF16 (d in {64, 128} for F32), N >= 1, K >= 0.
+ */
+sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t *topk_idxs,
+                              const float *sinks, sattn_sink_mode sink_mode, float scale, void *o,
+                              float *lse, int32_t B, int32_t M, int32_t H, int32_t d, int32_t N,
+                              int32_t K, void *workspace, size_t workspace_bytes,
+                              sattn_dtype dtype, void *cuda_stream);
+
+/* Workspace size (bytes) that lets sattn_sparse_fwd split each index list. */
+size_t sattn_sparse_workspace_bytes(int32_t B, int32_t M, int32_t H, int32_t d, int32_t K);
+
+/*
+ * Merge of chunk partials through their log-sum-exp ("XAttention Offload
+ * Stream Synchronization Fix", technical details: partial (m_i, l_i) stats per
+ * KV chunk, merged into (m_global, l_global), outputs normalised with them).
+ *
+ *   o_parts float32 [C, R, d] (each normalised within its chunk),
+ *   lse_parts float32 [C, R] (-inf for a chunk in which the row saw nothing)
+ *   sinks float32 [H] or NULL: a null-logit term exp(sinks[r % H]) is added
+ *     to the merged denominator exactly once.
+ *   o [R, d] (dtype), lse [R] float32 or NULL.
+ *   lse = ln(sum_c exp(lse_c) [+ exp(sink)]),  o = sum_c exp(lse_c - lse) o_c.
+ * A row with every lse_c = -inf and no sink gives o = 0, lse = -inf.
+ */
+sattn_status sattn_merge_lse(const float *o_parts, const float *lse_parts, int32_t C, int64_t R,
+                             int32_t d, int32_t H, const float *sinks, void *o, float *lse,
+                             sattn_dtype dtype, void *cuda_stream);
+
+/*
+ * One KV chunk of block-sparse causal attention (same nano-vllm page: chunked
+ * KV with per-chunk partial stats; test results give ~10% block density).
+ *
+ *   q [M, H, d] at absolute positions q_pos0 .. q_pos0 + M - 1,
+ *   k/v [Nctx, Hkv, d],
+ *   block_mask uint8 [H, ceil(M/128), ceil(Nctx/128)]: entry [h][i/128][j/128]
+ *     != 0 lets query i of head h see key j (query blocks local, key blocks
+ *     absolute);
+ *   only keys in [kv_begin, kv_end) are used; with causal, key j needs
+ *     j <= q_pos0 + i.
+ *   o_part float32 [M, H, d] normalised within the chunk, lse_part float32
+ *   [M, H] (-inf where the row sees nothing in the chunk; o_part is then 0).
+ * Merge the chunks with sattn_merge_lse (C = number of chunks, R = M * H).
+ * Requirements: H % Hkv == 0, dtype BF16 with d == 128 or F32 with d in {64, 128},
+ *   0 <= kv_begin <= kv_end <= Nctx.
+ */
+sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,
+                                    const uint8_t *block_mask, int32_t M, int32_t Nctx, int32_t H,
+                                    int32_t Hkv, int32_t d, int32_t q_pos0, int32_t kv_begin,
+                                    int32_t kv_end, int32_t causal, float scale, float *o_part,
+                                    float *lse_part, sattn_dtype dtype, void *cuda_stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *sattn_status_str(sattn_status s);
+
+/* Debug mode: every compute call synchronises its stream and reports the
+ * device error word (SATTN_ERR_DEVICE_CHECK / SATTN_ERR_TIMEOUT). */
+void sattn_set_debug(int on);
+
+/* Synchronise `cuda_stream`, then read and clear the device error word of the
+ * current device. Returns SATTN_OK, SATTN_ERR_DEVICE_CHECK, SATTN_ERR_TIMEOUT
+ * or SATTN_ERR_CUDA. */
+sattn_status sattn_check_device(void *cuda_stream);
+
+/* Upper bound, in nanoseconds, on any single wait inside a kernel (default
+ * one second). A value of 0 restores the default. */
+void sattn_set_wait_limit_ns(uint64_t ns);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t sattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SATTN_H_ */

@@ -1,0 +1,104 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+symbol that include/sattn.h declares; invalid arguments are rejected on the
+host before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(sattn_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from windowed_attention_sinks_gb300 import build
+
+    build.build()
+    import windowed_attention_sinks_gb300 as sa
+
+    return sa.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("sattn_window_fwd", "sattn_sparse_fwd", "sattn_merge_lse",
+              "sattn_block_sparse_fwd", "sattn_sparse_workspace_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in sorted(_declared()):
+        assert hasattr(lib, n), "missing export %s" % n
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        assert lib.sattn_status_str(code)
+    assert lib.sattn_version() >= 100
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    # H % Hkv != 0
+    rc = lib.sattn_window_fwd(fake, fake, fake, fake, None, fake, 1, 10, 10, 6, 4, 128, 8, 8, 0,
+                              None, 0, 0.1, 1, None)
+    assert rc == 1
+    # d not in {64, 128}
+    rc = lib.sattn_window_fwd(fake, fake, fake, fake, None, fake, 1, 10, 10, 8, 4, 96, 8, 8, 0,
+                              None, 0, 0.1, 1, None)
+    assert rc == 1
+    # sink mode without sinks
+    rc = lib.sattn_window_fwd(fake, fake, fake, fake, None, fake, 1, 10, 10, 8, 4, 128, 8, 8, 0,
+                              None, 1, 0.1, 1, None)
+    assert rc == 1
+    # NaN scale
+    rc = lib.sattn_window_fwd(fake, fake, fake, fake, None, fake, 1, 10, 10, 8, 4, 128, 8, 8, 0,
+                              None, 0, float("nan"), 1, None)
+    assert rc == 1
+    # NULL q
+    rc = lib.sattn_window_fwd(None, fake, fake, fake, None, fake, 1, 10, 10, 8, 4, 128, 8, 8, 0,
+                              None, 0, 0.1, 1, None)
+    assert rc == 1
+    # empty work is a no-op
+    rc = lib.sattn_window_fwd(None, None, None, None, None, None, 0, 0, 0, 8, 4, 128, 8, 8, 0,
+                              None, 0, 0.1, 1, None)
+    assert rc == 0
+    # sparse: negative K, misaligned workspace, bf16 with d=64
+    rc = lib.sattn_sparse_fwd(fake, fake, fake, None, 0, 0.1, fake, None, 1, 1, 32, 128, 10, -1,
+                              None, 0, 1, None)
+    assert rc == 1
+    rc = lib.sattn_sparse_fwd(fake, fake, fake, None, 0, 0.1, fake, None, 1, 1, 32, 128, 10, 5,
+                              P(0x1004), 4096, 1, None)
+    assert rc == 1
+    rc = lib.sattn_sparse_fwd(fake, fake, fake, None, 0, 0.1, fake, None, 1, 1, 32, 64, 10, 5,
+                              None, 0, 1, None)
+    assert rc == 2
+    rc = lib.sattn_sparse_fwd(None, None, None, None, 0, 0.1, None, None, 0, 5, 32, 128, 10, 5,
+                              None, 0, 1, None)
+    assert rc == 0
+    # block sparse: kv range outside the context
+    rc = lib.sattn_block_sparse_fwd(fake, fake, fake, fake, 4, 100, 8, 4, 128, 0, 0, 101, 1, 0.1,
+                                    fake, fake, 1, None)
+    assert rc == 1
+    # merge: bad d
+    rc = lib.sattn_merge_lse(fake, fake, 2, 10, 0, 8, None, fake, None, 0, None)
+    assert rc == 1
+
+
+def test_workspace_size_monotone(lib):
+    small = lib.sattn_sparse_workspace_bytes(1, 1, 32, 128, 640)
+    big = lib.sattn_sparse_workspace_bytes(64, 1, 32, 128, 640)
+    assert big >= small >= 0
+    assert lib.sattn_sparse_workspace_bytes(0, 1, 32, 128, 640) == 0

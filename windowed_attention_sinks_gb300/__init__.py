@@ -1,0 +1,210 @@
+"""sattn for GB300: index-gathered attention forward with sinks.
+
+A thin binding over libsattn.so (C ABI, include/sattn.h). The functions here
+only marshal torch tensors into device pointers, sizes and the current CUDA
+stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: if the library is missing or cannot load, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import workloads  # noqa: F401  (seeded input generators)
+
+SINK_NONE, SINK_KEY0_BIAS, SINK_NULL_LOGIT = 0, 1, 2
+F32, BF16 = 0, 1
+BLOCK = 128
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsattn.so")
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
+          4: "device check failed", 5: "device wait timed out"}
+
+_lib = None
+
+
+class SattnError(RuntimeError):
+    def __init__(self, fn, code):
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS.get(code, "?"), code))
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsattn.so (built by build.build()) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libsattn.so is not built; run windowed_attention_sinks_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                            ctypes.c_size_t)
+    L.sattn_window_fwd.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                   P, ctypes.c_int, f32, ctypes.c_int, P]
+    L.sattn_window_fwd.restype = ctypes.c_int
+    L.sattn_sparse_fwd.argtypes = [P, P, P, P, ctypes.c_int, f32, P, P, i32, i32, i32, i32, i32,
+                                   i32, P, sz, ctypes.c_int, P]
+    L.sattn_sparse_fwd.restype = ctypes.c_int
+    L.sattn_sparse_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    L.sattn_sparse_workspace_bytes.restype = sz
+    L.sattn_merge_lse.argtypes = [P, P, i32, i64, i32, i32, P, P, P, ctypes.c_int, P]
+    L.sattn_merge_lse.restype = ctypes.c_int
+    L.sattn_block_sparse_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                         f32, P, P, ctypes.c_int, P]
+    L.sattn_block_sparse_fwd.restype = ctypes.c_int
+    L.sattn_status_str.argtypes = [ctypes.c_int]
+    L.sattn_status_str.restype = ctypes.c_char_p
+    L.sattn_set_debug.argtypes = [ctypes.c_int]
+    L.sattn_set_debug.restype = None
+    L.sattn_check_device.argtypes = [P]
+    L.sattn_check_device.restype = ctypes.c_int
+    L.sattn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    L.sattn_set_wait_limit_ns.restype = None
+    L.sattn_version.restype = i32
+    _lib = L
+    return L
+
+
+def _check(fn, code):
+    if code != 0:
+        raise SattnError(fn, code)
+
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _need(t, name, dtype=None, device=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s" % (name, dtype))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, expected %s" % (name, t.device, device))
+
+
+def window_fwd(q, k, v, cu_seqlens, max_seqlen, window_left, window_right, causal=False,
+               sinks=None, sink_mode=SINK_NONE, scale=None, o=None, lse=None, stream=None):
+    """Sliding-window varlen attention (sattn_window_fwd). Returns (o, lse)."""
+    import torch
+
+    T, H, d = q.shape
+    Hkv = k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, q.device)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, q.device)
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
+    scale = float(d ** -0.5 if scale is None else scale)
+    code = lib().sattn_window_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_seqlens),
+                                  cu_seqlens.numel() - 1, T, int(max_seqlen), H, Hkv, d,
+                                  int(window_left), int(window_right), int(bool(causal)),
+                                  _ptr(sinks), int(sink_mode), scale, _dtype_code(q),
+                                  _stream(stream))
+    _check("sattn_window_fwd", code)
+    return o, lse
+
+
+def sparse_workspace_bytes(B, M, H, d, K):
+    return int(lib().sattn_sparse_workspace_bytes(B, M, H, d, K))
+
+
+def sparse_fwd(q, kv_cache, topk_idxs, sinks=None, sink_mode=SINK_NONE, scale=None, o=None,
+               lse=None, workspace=None, stream=None):
+    """Gathered attention over one shared KV head (sattn_sparse_fwd). Returns (o, lse)."""
+    import torch
+
+    B, M, H, d = q.shape
+    N = kv_cache.shape[1]
+    K = topk_idxs.shape[2]
+    _need(q, "q", None, q.device)
+    _need(kv_cache, "kv_cache", q.dtype, q.device)
+    _need(topk_idxs, "topk_idxs", torch.int32, q.device)
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, M, H), dtype=torch.float32, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = float(d ** -0.5 if scale is None else scale)
+    code = lib().sattn_sparse_fwd(_ptr(q), _ptr(kv_cache), _ptr(topk_idxs), _ptr(sinks),
+                                  int(sink_mode), scale, _ptr(o), _ptr(lse), B, M, H, d, N, K,
+                                  _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
+    _check("sattn_sparse_fwd", code)
+    return o, lse
+
+
+def merge_lse(o_parts, lse_parts, H, sinks=None, out_dtype=None, o=None, lse=None, stream=None):
+    """LSE merge of chunk partials (sattn_merge_lse). o_parts[C,R,d], lse_parts[C,R] fp32."""
+    import torch
+
+    C, R, d = o_parts.shape
+    _need(o_parts, "o_parts", torch.float32)
+    _need(lse_parts, "lse_parts", torch.float32, o_parts.device)
+    if o is None:
+        o = torch.empty((R, d), dtype=out_dtype or torch.float32, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty((R,), dtype=torch.float32, device=o_parts.device)
+    code = lib().sattn_merge_lse(_ptr(o_parts), _ptr(lse_parts), C, R, d, H, _ptr(sinks), _ptr(o),
+                                 _ptr(lse), _dtype_code(o), _stream(stream))
+    _check("sattn_merge_lse", code)
+    return o, lse
+
+
+def block_sparse_fwd(q, k, v, block_mask, q_pos0, kv_begin, kv_end, causal=True, scale=None,
+                     o_part=None, lse_part=None, stream=None):
+    """One KV chunk of block-sparse attention (sattn_block_sparse_fwd). Returns fp32 partials."""
+    import torch
+
+    M, H, d = q.shape
+    Nctx, Hkv = k.shape[0], k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, q.device)
+    _need(block_mask, "block_mask", torch.uint8, q.device)
+    if o_part is None:
+        o_part = torch.empty((M, H, d), dtype=torch.float32, device=q.device)
+    if lse_part is None:
+        lse_part = torch.empty((M, H), dtype=torch.float32, device=q.device)
+    scale = float(d ** -0.5 if scale is None else scale)
+    code = lib().sattn_block_sparse_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_mask), M, Nctx, H,
+                                        Hkv, d, int(q_pos0), int(kv_begin), int(kv_end),
+                                        int(bool(causal)), scale, _ptr(o_part), _ptr(lse_part),
+                                        _dtype_code(q), _stream(stream))
+    _check("sattn_block_sparse_fwd", code)
+    return o_part, lse_part
+
+
+def check_device(stream=None):
+    """Synchronise and read/clear the device error word; raises on a recorded error."""
+    _check("sattn_check_device", lib().sattn_check_device(_stream(stream)))
+
+
+def set_debug(on: bool):
+    lib().sattn_set_debug(1 if on else 0)

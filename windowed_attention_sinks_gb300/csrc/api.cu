@@ -1,0 +1,261 @@
+// C ABI of libsattn.so: argument validation, per-device set-up and dispatch
+// to the kernel launchers. No exception crosses this boundary and nothing is
+// allocated: the only device memory the library owns is the error word below,
+// a module-scope variable.
+#include <atomic>
+#include <mutex>
+#include <new>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace sattn {
+
+__device__ unsigned g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+DevInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+std::atomic<int> g_debug{0};
+std::atomic<uint64_t> g_wait_ns{1000000000ull};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaStream_t as_stream(void *s) {
+    return s ? static_cast<cudaStream_t>(s) : cudaStreamPerThread;
+}
+
+sattn_status finish(cudaError_t e, cudaStream_t s) {
+    if (e != cudaSuccess) return SATTN_ERR_CUDA;
+    if (g_debug.load()) return sattn_check_device(s);
+    return SATTN_OK;
+}
+
+bool is_device_ptr(const void *p) { return p != nullptr; }
+
+}  // namespace
+
+const DevInfo *device_info(cudaError_t *e) {
+    int dev = -1;
+    *e = cudaGetDevice(&dev);
+    if (*e != cudaSuccess) return nullptr;
+    if (dev < 0 || dev >= kMaxDevices) {
+        *e = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DevInfo d;
+        d.device = dev;
+        if ((*e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+            return nullptr;
+        if ((*e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess)
+            return nullptr;
+        if ((*e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+            cudaSuccess)
+            return nullptr;
+        void *p = nullptr;
+        if ((*e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return nullptr;
+        d.err = static_cast<unsigned *>(p);
+        if ((*e = cudaMemset(d.err, 0, sizeof(unsigned))) != cudaSuccess) return nullptr;
+        if ((*e = cudaDeviceSynchronize()) != cudaSuccess) return nullptr;
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    return &g_dev[dev];
+}
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+
+CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank, void *base,
+                           const uint64_t *dims, const uint64_t *strides_bytes,
+                           const uint32_t *box, CUtensorMapSwizzle swizzle) {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    if (!g_encode) return CUDA_ERROR_NOT_FOUND;
+    cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    return g_encode(map, dtype, rank, base, reinterpret_cast<const cuuint64_t *>(dims),
+                    reinterpret_cast<const cuuint64_t *>(strides_bytes),
+                    reinterpret_cast<const cuuint32_t *>(box), estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace sattn
+
+using namespace sattn;
+
+namespace {
+
+bool valid_dtype(sattn_dtype t) { return t == SATTN_F32 || t == SATTN_BF16; }
+bool valid_sink(sattn_sink_mode m, const float *sinks) {
+    if (m == SATTN_SINK_NONE) return true;
+    if (m != SATTN_SINK_KEY0_BIAS && m != SATTN_SINK_NULL_LOGIT) return false;
+    return sinks != nullptr;
+}
+bool finite_scale(float s) { return s == s && s - s == 0.0f; }
+
+// sm_103 only: the fatbin carries sm_103a code and nothing else.
+sattn_status check_arch(const DevInfo *dev) {
+    if (dev->cc_major != 10 || dev->cc_minor != 3) return SATTN_ERR_UNSUPPORTED;
+    return SATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sattn_version(void) { return 100; }
+
+const char *sattn_status_str(sattn_status s) {
+    switch (s) {
+    case SATTN_OK: return "ok";
+    case SATTN_ERR_INVALID_ARG: return "invalid argument";
+    case SATTN_ERR_UNSUPPORTED: return "unsupported device or argument combination";
+    case SATTN_ERR_CUDA: return "CUDA error";
+    case SATTN_ERR_DEVICE_CHECK: return "device-side index or sequence check failed";
+    case SATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+void sattn_set_debug(int on) { g_debug.store(on ? 1 : 0); }
+
+void sattn_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : 1000000000ull); }
+
+sattn_status sattn_check_device(void *cuda_stream) {
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    cudaStream_t s = as_stream(cuda_stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SATTN_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SATTN_ERR_CUDA;
+    if (word) {
+        unsigned zero = 0;
+        if (cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return SATTN_ERR_CUDA;
+    }
+    if (word & DEVERR_TIMEOUT) return SATTN_ERR_TIMEOUT;
+    if (word) return SATTN_ERR_DEVICE_CHECK;
+    return SATTN_OK;
+}
+
+sattn_status sattn_window_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                              int32_t max_seqlen, int32_t H, int32_t Hkv, int32_t d,
+                              int32_t window_left, int32_t window_right, int32_t causal,
+                              const float *sinks, sattn_sink_mode sink_mode, float scale,
+                              sattn_dtype dtype, void *cuda_stream) {
+    if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return SATTN_ERR_INVALID_ARG;
+    if (H <= 0 || Hkv <= 0 || H % Hkv != 0) return SATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return SATTN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_sink(sink_mode, sinks) || !finite_scale(scale))
+        return SATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return SATTN_ERR_INVALID_ARG;
+    if (total_tokens == 0 || num_seqs == 0) return SATTN_OK;
+    if (max_seqlen == 0) return SATTN_ERR_INVALID_ARG;
+    if (!is_device_ptr(q) || !is_device_ptr(k) || !is_device_ptr(v) || !is_device_ptr(o) ||
+        !is_device_ptr(cu_seqlens))
+        return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    WindowArgs a{q, k, v, o, lse, cu_seqlens, num_seqs, total_tokens, max_seqlen, H, Hkv, d,
+                 window_left < 0 ? -1 : window_left, window_right < 0 ? -1 : window_right,
+                 causal, sink_mode == SATTN_SINK_NONE ? nullptr : sinks, (int)sink_mode, scale,
+                 (int)dtype};
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_window_simt(a, *dev, s), s);
+}
+
+size_t sattn_sparse_workspace_bytes(int32_t B, int32_t M, int32_t H, int32_t d, int32_t K) {
+    if (B <= 0 || M <= 0 || H <= 0 || d <= 0 || K <= 0) return 0;
+    return 0;
+}
+
+sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t *topk_idxs,
+                              const float *sinks, sattn_sink_mode sink_mode, float scale, void *o,
+                              float *lse, int32_t B, int32_t M, int32_t H, int32_t d, int32_t N,
+                              int32_t K, void *workspace, size_t workspace_bytes,
+                              sattn_dtype dtype, void *cuda_stream) {
+    if (B < 0 || M < 0 || H <= 0 || N < 0 || K < 0) return SATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return SATTN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !valid_sink(sink_mode, sinks) || !finite_scale(scale))
+        return SATTN_ERR_INVALID_ARG;
+    if (B == 0 || M == 0) return SATTN_OK;
+    if (N == 0) return SATTN_ERR_INVALID_ARG;
+    if (!q || !kv_cache || !o || (K > 0 && !topk_idxs)) return SATTN_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SATTN_ERR_INVALID_ARG;
+    if (dtype == SATTN_BF16 && d != 128) return SATTN_ERR_UNSUPPORTED;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    SparseArgs a{q, kv_cache, topk_idxs, sink_mode == SATTN_SINK_NONE ? nullptr : sinks,
+                 (int)sink_mode, scale, o, lse, B, M, H, d, N, K, workspace, workspace_bytes,
+                 (int)dtype};
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_sparse_simt(a, *dev, s), s);
+}
+
+sattn_status sattn_merge_lse(const float *o_parts, const float *lse_parts, int32_t C, int64_t R,
+                             int32_t d, int32_t H, const float *sinks, void *o, float *lse,
+                             sattn_dtype dtype, void *cuda_stream) {
+    if (C < 0 || R < 0 || d <= 0 || d > 1024 || H <= 0 || !valid_dtype(dtype))
+        return SATTN_ERR_INVALID_ARG;
+    if (R == 0) return SATTN_OK;
+    if ((C > 0 && (!o_parts || !lse_parts)) || !o) return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    MergeArgs a{o_parts, lse_parts, C, R, d, H, sinks, o, lse, (int)dtype};
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_merge(a, *dev, s), s);
+}
+
+sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,
+                                    const uint8_t *block_mask, int32_t M, int32_t Nctx, int32_t H,
+                                    int32_t Hkv, int32_t d, int32_t q_pos0, int32_t kv_begin,
+                                    int32_t kv_end, int32_t causal, float scale, float *o_part,
+                                    float *lse_part, sattn_dtype dtype, void *cuda_stream) {
+    if (M < 0 || Nctx < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0) return SATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return SATTN_ERR_INVALID_ARG;
+    if (q_pos0 < 0 || kv_begin < 0 || kv_end > Nctx || kv_begin > kv_end)
+        return SATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return SATTN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !finite_scale(scale)) return SATTN_ERR_INVALID_ARG;
+    if (M == 0) return SATTN_OK;
+    if (!q || !o_part || !lse_part || (Nctx > 0 && (!k || !v || !block_mask)))
+        return SATTN_ERR_INVALID_ARG;
+    if (dtype == SATTN_BF16 && d != 128) return SATTN_ERR_UNSUPPORTED;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    BlockArgs a{q, k, v, block_mask, M, Nctx, H, Hkv, d, q_pos0, kv_begin, kv_end, causal, scale,
+                o_part, lse_part, (int)dtype};
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_block_simt(a, *dev, s), s);
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Host-side interface between the C ABI (api.cu) and the kernel launchers.
+// Arguments reaching a launcher have already been validated.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sattn.h"
+
+namespace sattn {
+
+struct DevInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    unsigned *err = nullptr;  // device address of the error word
+};
+
+// Per-device facts, initialised once per device (thread-safe).
+const DevInfo *device_info(cudaError_t *e);
+uint64_t wait_limit_ns();
+
+// cuTensorMapEncodeTiled through the driver entry point (no libcuda link).
+CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank,
+                           void *base, const uint64_t *dims, const uint64_t *strides_bytes,
+                           const uint32_t *box, CUtensorMapSwizzle swizzle);
+
+struct WindowArgs {
+    const void *q, *k, *v;
+    void *o;
+    float *lse;
+    const int32_t *cu_seqlens;
+    int num_seqs, T, max_seqlen, H, Hkv, d, wl, wr, causal;
+    const float *sinks;
+    int sink_mode;
+    float scale;
+    int dtype;
+};
+
+struct SparseArgs {
+    const void *q, *kv;
+    const int32_t *idx;
+    const float *sinks;
+    int sink_mode;
+    float scale;
+    void *o;
+    float *lse;
+    int B, M, H, d, N, K;
+    void *workspace;
+    size_t workspace_bytes;
+    int dtype;
+};
+
+struct BlockArgs {
+    const void *q, *k, *v;
+    const uint8_t *mask;
+    int M, Nctx, H, Hkv, d, q_pos0, kv_begin, kv_end, causal;
+    float scale;
+    float *o_part, *lse_part;
+    int dtype;
+};
+
+struct MergeArgs {
+    const float *o_parts, *lse_parts;
+    int C;
+    int64_t R;
+    int d, H;
+    const float *sinks;
+    void *o;
+    float *lse;
+    int dtype;
+};
+
+// SIMT kernels: any dtype, d in {64, 128}.
+cudaError_t launch_window_simt(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_sparse_simt(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_block_simt(const BlockArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s);
+
+// tcgen05 kernels: bf16, d = 128.
+cudaError_t launch_window_tc(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
+size_t sparse_tc_workspace_bytes(int B, int M, int H, int d, int K);
+
+}  // namespace sattn
