@@ -1,0 +1,525 @@
+#!/usr/bin/env python
+"""Throughput benchmark for index-gathered attention with sinks on GB300.
+
+Default workload: the windowed vision-encoder attention (bf16): 256 varlen
+sequences with lengths ~ U{64..1024}, 16 query heads, head dim 128, window 128,
+non-causal. One step runs the whole workload: both KV-head counts (16 and 8)
+and both sink semantics (key-0 bias and null logit), four launches of
+sattn_window_fwd over device-resident inputs. The metric is queries/s (query
+tokens per second, all four passes counted).
+
+Other workloads (--workload decode | prefill | block) measure the gathered
+decode / prefill and the chunked block-sparse paths the same way.
+
+Output: one JSON line on rank 0. Timing: W warm-up steps, then K steps between
+a barrier + device synchronisation on both sides, CUDA events on the launch
+stream around every launch; inputs are larger than L2 (config "l2" says
+which).
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                  "sw_power_cap"), parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+
+def window_work(seed):
+    """Both KV-head variants and both sink modes of the vision workload."""
+    from windowed_attention_sinks_gb300 import workloads as W
+
+    passes = []
+    for hkv in (16, 8):
+        case = W.window_vision_bf16(seed, hkv)
+        for mode in (W.SINK_KEY0_BIAS, W.SINK_NULL_LOGIT):
+            passes.append((case, mode))
+    return passes
+
+
+def window_counts(case):
+    """Algorithmic bytes and FLOPs of one window pass over the workload."""
+    lens = np.diff(case.cu_seqlens).astype(np.int64)
+    T, H, Hkv, d, w = case.T, case.H, case.Hkv, case.d, case.window_left
+    pairs = 0
+    for L in lens:
+        i = np.arange(L)
+        pairs += int((np.minimum(L - 1, i + w) - np.maximum(0, i - w) + 1).sum())
+    bytes_ = 2 * T * H * d * 2 + 2 * T * Hkv * d * 2 + T * H * 4
+    flops = 4 * d * pairs * H
+    return bytes_, flops
+
+
+def run_sattn(args, rank, world, device):
+    import torch
+
+    import windowed_attention_sinks_gb300 as sa
+
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream()
+    peaks, peaks_src = load_peaks()
+    seed = 1000 + rank  # each rank owns an independent batch (weak scaling)
+    if args.workload != "window":
+        return run_other(args, rank, world, device, peaks, peaks_src)
+
+    passes = window_work(seed)
+    dev_inputs = {}
+    launches = []
+    total_q, total_bytes, total_flops = 0, 0, 0
+    for case, mode in passes:
+        key = id(case)
+        if key not in dev_inputs:
+            bf = torch.bfloat16
+            dev_inputs[key] = dict(
+                q=torch.from_numpy(case.q).to(bf).to(device),
+                k=torch.from_numpy(case.k).to(bf).to(device),
+                v=torch.from_numpy(case.v).to(bf).to(device),
+                cu=torch.from_numpy(case.cu_seqlens).to(device),
+                sinks=torch.from_numpy(case.sinks).to(device))
+            dev_inputs[key]["o"] = torch.empty_like(dev_inputs[key]["q"])
+            dev_inputs[key]["lse"] = torch.empty((case.T, case.H), dtype=torch.float32,
+                                                 device=device)
+        t = dev_inputs[key]
+        b, f = window_counts(case)
+        launches.append((case, mode, t, b, f))
+        total_q += case.T
+        total_bytes += b
+        total_flops += f
+
+    def one_step(events=None):
+        for i, (case, mode, t, _, _) in enumerate(launches):
+            if events is not None:
+                events[i][0].record(stream)
+            sa.window_fwd(t["q"], t["k"], t["v"], t["cu"], case.max_seqlen, case.window_left,
+                          case.window_right, False, t["sinks"], mode, case.scale,
+                          o=t["o"], lse=t["lse"], stream=stream)
+            if events is not None:
+                events[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    sa.check_device(stream)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in launches] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index(device)) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s in range(args.steps):
+            one_step(ev[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    launch_ms = [[a.elapsed_time(b) for a, b in row] for row in ev]
+    avg_launch_ms = float(np.mean(launch_ms))
+    sa.check_device(stream)
+
+    ms_per_step = elapsed_ms / args.steps
+    value = total_q * world / (ms_per_step / 1e3)
+    achieved_gbs = total_bytes / (np.sum(launch_ms) / args.steps / 1e3) / 1e9
+    achieved_tf = total_flops / (np.sum(launch_ms) / args.steps / 1e3) / 1e12
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    out = {
+        "metric": "queries/s (window attention, bf16, 256 varlen seqs, H=16, Hkv 16+8, "
+                  "d=128, w=128, key0_bias+null_logit)",
+        "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64, bf16)",
+        "config": {"workload": "window-vision-bf16: 256 seqs U{64..1024}, H=16, Hkv in {16,8}, "
+                               "d=128, w=128, non-causal, sinks key0_bias and null_logit "
+                               "(4 launches per step)",
+                   "tokens_per_pass": int(launches[0][0].T), "launches_per_step": len(launches),
+                   "l2": "inputs larger than L2 (1.7-2.3 GB per launch), no flush",
+                   "parallelism": "replicas (dp%d, independent batches)" % world},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "traffic": None,
+                     "peak_source": peaks_src,
+                     "kernel": "attn_tc_kernel<window>", "avg_launch_ms": avg_launch_ms,
+                     "tflops": achieved_tf,
+                     "tensor_frac": achieved_tf / peaks.get("bf16_tflops_sustained", 1700.0)},
+        "gpu_launches": len(launches) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        out["e2e"] = e2e_window(args, launches, device, stream)
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_window(launches)
+    return out
+
+
+def e2e_window(args, launches, device, stream):
+    """Same metric through the public API with host buffers: every step copies
+    q/k/v/cu/sinks host->device (pinned) and o/lse device->host."""
+    import torch
+
+    import windowed_attention_sinks_gb300 as sa
+
+    host = []
+    h2d = d2h = 0
+    for case, mode, t, _, _ in launches:
+        hq = t["q"].cpu().pin_memory()
+        hk = t["k"].cpu().pin_memory()
+        hv = t["v"].cpu().pin_memory()
+        hcu = t["cu"].cpu().pin_memory()
+        hs = t["sinks"].cpu().pin_memory()
+        ho = torch.empty_like(hq).pin_memory()
+        hl = torch.empty(t["lse"].shape, dtype=torch.float32).pin_memory()
+        host.append((case, mode, t, hq, hk, hv, hcu, hs, ho, hl))
+        h2d += sum(x.numel() * x.element_size() for x in (hq, hk, hv, hcu, hs))
+        d2h += ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def step():
+        for case, mode, t, hq, hk, hv, hcu, hs, ho, hl in host:
+            t["q"].copy_(hq, non_blocking=True)
+            t["k"].copy_(hk, non_blocking=True)
+            t["v"].copy_(hv, non_blocking=True)
+            t["cu"].copy_(hcu, non_blocking=True)
+            t["sinks"].copy_(hs, non_blocking=True)
+            sa.window_fwd(t["q"], t["k"], t["v"], t["cu"], case.max_seqlen, case.window_left,
+                          case.window_right, False, t["sinks"], mode, case.scale,
+                          o=t["o"], lse=t["lse"], stream=stream)
+            ho.copy_(t["o"], non_blocking=True)
+            hl.copy_(t["lse"], non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    q = sum(c.T for c, *_ in host)
+    return {"value": q / dt, "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps}
+
+
+def cpu_baseline_window(launches, budget_s=15.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the same workload:
+    whole sequences (all heads) until ~budget_s of CPU work is spent."""
+    import oracle
+
+    oracle.build()
+    cores = oracle.get_threads()
+    done_q, spent, seqs = 0, 0.0, 0
+    case, mode = launches[0][0], launches[0][1]
+    lens = np.diff(case.cu_seqlens)
+    t_start = time.perf_counter()
+    for s in range(len(lens)):
+        a, b = int(case.cu_seqlens[s]), int(case.cu_seqlens[s + 1])
+        rows = np.arange(a * case.H, b * case.H, dtype=np.int64)
+        oracle.window(case.q, case.k, case.v, case.cu_seqlens, case.H, case.Hkv, case.d,
+                      case.window_left, case.window_right, 0, case.sinks, mode, case.scale,
+                      rows=rows)
+        done_q += b - a
+        seqs += 1
+        spent = time.perf_counter() - t_start
+        if spent > budget_s:
+            break
+    return {"value": done_q / spent, "unit": "queries/s", "cores": cores, "kind": "oracle",
+            "sample": "%d of 256 sequences (%d query tokens x 16 heads) of the Hkv=16 key0_bias "
+                      "pass, fp64, %.1f s" % (seqs, done_q, spent)}
+
+
+def run_other(args, rank, world, device, peaks, peaks_src):
+    """Decode / prefill / block-sparse measurement lines (same JSON shape)."""
+    import torch
+
+    import windowed_attention_sinks_gb300 as sa
+    from windowed_attention_sinks_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream()
+    bf = torch.bfloat16
+    seed = 1000 + rank
+    if args.workload in ("decode", "prefill"):
+        case = W.sparse_decode_bf16(seed) if args.workload == "decode" else \
+            W.sparse_prefill_bf16(seed)
+        q = torch.from_numpy(case.q).to(bf).to(device)
+        kv = torch.from_numpy(case.kv).to(bf).to(device)
+        idx = torch.from_numpy(case.idx).to(device)
+        sinks = torch.from_numpy(case.sinks).to(device)
+        o = torch.empty_like(q)
+        lse = torch.empty((case.B, case.M, case.H), dtype=torch.float32, device=device)
+        nb = sa.sparse_workspace_bytes(case.B, case.M, case.H, case.d, case.K)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
+        valid = int((case.idx >= 0).sum())
+        nbytes = valid * case.d * 2 + case.idx.size * 4 + 2 * q.numel() * 2 + lse.numel() * 4
+        flops = 4 * case.d * valid * case.H
+        units = case.B * case.M
+        # decode is tiny: a scratch buffer larger than L2 is rewritten before every launch
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) \
+            if args.workload == "decode" else None
+
+        def launch():
+            sa.sparse_fwd(q, kv, idx, sinks, case.sink_mode, case.scale, o=o, lse=lse,
+                          workspace=ws, stream=stream)
+        name = "sparse %s bf16: B=%d M=%d H=%d d=%d N=%d K=%d null_logit" % (
+            args.workload, case.B, case.M, case.H, case.d, case.N, case.K)
+    else:
+        case = W.block_sparse_bf16(seed)
+        q = torch.from_numpy(case.q).to(bf).to(device)
+        k = torch.from_numpy(case.k).to(bf).to(device)
+        v = torch.from_numpy(case.v).to(bf).to(device)
+        mask = torch.from_numpy(case.mask).to(device)
+        C = len(case.chunks)
+        op = torch.empty((C, case.M * case.H, case.d), dtype=torch.float32, device=device)
+        lp = torch.empty((C, case.M * case.H), dtype=torch.float32, device=device)
+        o = torch.empty((case.M * case.H, case.d), dtype=bf, device=device)
+        lse = torch.empty((case.M * case.H,), dtype=torch.float32, device=device)
+        nblk = int(case.mask.sum())
+        nbytes = (q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + 2 * op.numel() * 4
+                  + 2 * lp.numel() * 4 + o.numel() * 2 + lse.numel() * 4)
+        # causal pairs inside kept blocks (diagonal blocks are half visible)
+        flops = 4 * case.d * (nblk * 128 * 128 - case.H * (case.M // 128) * (128 * 127 // 2))
+        units = case.M
+        flush = None
+
+        def launch():
+            for c, (a, b) in enumerate(case.chunks):
+                sa.block_sparse_fwd(q, k, v, mask, case.q_pos0, a, b, True, case.scale,
+                                    o_part=op[c].view(case.M, case.H, case.d),
+                                    lse_part=lp[c].view(case.M, case.H), stream=stream)
+            sa.merge_lse(op, lp, case.H, o=o, lse=lse, stream=stream)
+        name = "block-sparse bf16: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 chunks + merge"
+
+    for _ in range(args.warmup):
+        launch()
+    sa.check_device(stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index(device)) as clk:
+        for s in range(args.steps):
+            if flush is not None:
+                flush.fill_(s & 0xff)
+            evs[s][0].record(stream)
+            launch()
+            evs[s][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    times = [a.elapsed_time(b) for a, b in evs]
+    ms = max_over_ranks(float(np.mean(times)), world)
+    sa.check_device(stream)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tf = flops / (ms / 1e3) / 1e12
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {
+        "metric": "queries/s (%s)" % args.workload, "value": units * world / (ms / 1e3),
+        "unit": "queries/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded numpy PCG64, bf16)",
+        "config": {"workload": name,
+                   "l2": "scratch > L2 rewritten before each step" if flush is not None
+                   else "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / peak, "traffic": None, "peak_source": peaks_src,
+                     "tflops": tf,
+                     "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
+        "gpu_launches": args.steps * (1 if args.workload != "block" else len(case.chunks) + 1),
+        "clocks": clk.summary(),
+    }
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    """The fp64 oracle timed on the host cores: each step is a bounded sample
+    (two whole sequences, all heads, one pass) of the default workload."""
+    import oracle
+    from windowed_attention_sinks_gb300 import workloads as W
+
+    if rank != 0:
+        return None
+    oracle.build()
+    case = W.window_vision_bf16(1000, 16)
+    lens = np.diff(case.cu_seqlens)
+
+    def step(s):
+        a = int(case.cu_seqlens[(2 * s) % 256])
+        b = int(case.cu_seqlens[(2 * s) % 256 + 2])
+        rows = np.arange(a * case.H, b * case.H, dtype=np.int64)
+        oracle.window(case.q, case.k, case.v, case.cu_seqlens, case.H, case.Hkv, case.d,
+                      case.window_left, case.window_right, 0, case.sinks, 1, case.scale,
+                      rows=rows)
+        return b - a
+
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    q = sum(step(args.warmup + s) for s in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = q / dt
+    cores = oracle.get_threads()
+    sample = "two whole sequences (all 16 heads) of the Hkv=16 key0_bias pass per step, fp64"
+    return {"impl": "reference", "metric": "queries/s (window attention, bf16, 256 varlen seqs, "
+            "H=16, Hkv 16+8, d=128, w=128, key0_bias+null_logit)",
+            "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy PCG64, bf16 inputs)",
+            "config": {"workload": "window-vision-bf16: 256 seqs U{64..1024}, H=16, Hkv in "
+                                   "{16,8}, d=128, w=128 (oracle sample)"},
+            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def gpu_index(device):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v for v in vis.split(",") if v.strip()]
+        if device < len(ids) and ids[device].strip().isdigit():
+            return int(ids[device])
+    return device
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="sattn", choices=["sattn", "reference"])
+    ap.add_argument("--workload", default="window", choices=["window", "decode", "prefill",
+                                                              "block"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    import torch
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    from windowed_attention_sinks_gb300 import build
+
+    build.build()
+    out = run_sattn(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

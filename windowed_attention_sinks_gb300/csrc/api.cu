@@ -110,6 +110,8 @@ bool valid_sink(sattn_sink_mode m, const float *sinks) {
     return sinks != nullptr;
 }
 bool finite_scale(float s) { return s == s && s - s == 0.0f; }
+// TMA tiles need 16-byte aligned base addresses.
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // sm_103 only: the fatbin carries sm_103a code and nothing else.
 sattn_status check_arch(const DevInfo *dev) {
@@ -184,6 +186,11 @@ sattn_status sattn_window_fwd(const void *q, const void *k, const void *v, void 
                  causal, sink_mode == SATTN_SINK_NONE ? nullptr : sinks, (int)sink_mode, scale,
                  (int)dtype};
     cudaStream_t s = as_stream(cuda_stream);
+    if (dtype == SATTN_BF16 && d == 128) {
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+            return SATTN_ERR_INVALID_ARG;
+        return finish(launch_window_tc(a, *dev, s), s);
+    }
     return finish(launch_window_simt(a, *dev, s), s);
 }
 
@@ -255,6 +262,11 @@ sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,
     BlockArgs a{q, k, v, block_mask, M, Nctx, H, Hkv, d, q_pos0, kv_begin, kv_end, causal, scale,
                 o_part, lse_part, (int)dtype};
     cudaStream_t s = as_stream(cuda_stream);
+    if (dtype == SATTN_BF16) {
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part))
+            return SATTN_ERR_INVALID_ARG;
+        return finish(launch_block_tc(a, *dev, s), s);
+    }
     return finish(launch_block_simt(a, *dev, s), s);
 }
 
