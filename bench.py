@@ -63,7 +63,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -105,13 +105,13 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- workloads
 
-def window_work(seed):
+def window_work(seed, num_seqs=256):
     """Both KV-head variants and both sink modes of the vision workload."""
     from windowed_attention_sinks_gb300 import workloads as W
 
     passes = []
     for hkv in (16, 8):
-        case = W.window_vision_bf16(seed, hkv)
+        case = W.window_vision_bf16(seed, hkv, num_seqs=num_seqs)
         for mode in (W.SINK_KEY0_BIAS, W.SINK_NULL_LOGIT):
             passes.append((case, mode))
     return passes
@@ -142,7 +142,7 @@ def run_sattn(args, rank, world, device):
     if args.workload != "window":
         return run_other(args, rank, world, device, peaks, peaks_src)
 
-    passes = window_work(seed)
+    passes = window_work(seed, args.seqs)
     dev_inputs = {}
     launches = []
     total_q, total_bytes, total_flops = 0, 0, 0
@@ -210,9 +210,9 @@ def run_sattn(args, rank, world, device):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64, bf16)",
-        "config": {"workload": "window-vision-bf16: 256 seqs U{64..1024}, H=16, Hkv in {16,8}, "
+        "config": {"workload": "window-vision-bf16: %d seqs U{64..1024}, H=16, Hkv in {16,8}, "
                                "d=128, w=128, non-causal, sinks key0_bias and null_logit "
-                               "(4 launches per step)",
+                               "(4 launches per step)" % args.seqs,
                    "tokens_per_pass": int(launches[0][0].T), "launches_per_step": len(launches),
                    "l2": "inputs larger than L2 (1.7-2.3 GB per launch), no flush",
                    "parallelism": "replicas (dp%d, independent batches)" % world},
@@ -443,7 +443,7 @@ def run_reference(args, rank, world):
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64, bf16 inputs)",
-            "config": {"workload": "window-vision-bf16: 256 seqs U{64..1024}, H=16, Hkv in "
+            "config": {"workload": "window-vision-bf16: %d seqs U{64..1024}, H=16, Hkv in "
                                    "{16,8}, d=128, w=128 (oracle sample)"},
             "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
@@ -484,11 +484,13 @@ def gpu_index(device):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="sattn", choices=["sattn", "reference"])
     ap.add_argument("--workload", default="window", choices=["window", "decode", "prefill",
                                                               "block"])
+    ap.add_argument("--seqs", type=int, default=256,
+                    help="window workload: number of sequences (256 = the full workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -78,7 +78,7 @@ typedef enum { SATTN_F32 = 0, SATTN_BF16 = 1 } sattn_dtype;
  * Query i sees key j iff both are in the same sequence and, with local
  * positions, -window_left <= j - i <= window_right (a negative bound means
  * unbounded on that side) and, if causal, j <= i. Query head h reads KV head
- * h / (H / Hkv). Logits are scale * <q, k>. o has q's dtype (round to
+ * h / (H / Hkv). Logits are scale * <q, k> with scale > 0. o has q's dtype (round to
  * nearest even for bf16). With dtype BF16 and d = 128 the tcgen05 kernel
  * runs; other combinations run the SIMT kernel.
  * Requirements: H % Hkv == 0, d in {64, 128}, num_seqs >= 0.

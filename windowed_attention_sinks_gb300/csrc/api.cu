@@ -2,6 +2,9 @@
 // to the kernel launchers. No exception crosses this boundary and nothing is
 // allocated: the only device memory the library owns is the error word below,
 // a module-scope variable.
+#include <stdio.h>
+#include <stdlib.h>
+
 #include <atomic>
 #include <mutex>
 #include <new>
@@ -34,7 +37,10 @@ cudaStream_t as_stream(void *s) {
 }
 
 sattn_status finish(cudaError_t e, cudaStream_t s) {
-    if (e != cudaSuccess) return SATTN_ERR_CUDA;
+    if (e != cudaSuccess) {
+        if (verbose()) fprintf(stderr, "sattn: CUDA error: %s\n", cudaGetErrorString(e));
+        return SATTN_ERR_CUDA;
+    }
     if (g_debug.load()) return sattn_check_device(s);
     return SATTN_OK;
 }
@@ -77,6 +83,11 @@ const DevInfo *device_info(cudaError_t *e) {
 
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
+bool verbose() {
+    static const bool v = getenv("SATTN_VERBOSE") != nullptr;
+    return v;
+}
+
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank, void *base,
                            const uint64_t *dims, const uint64_t *strides_bytes,
                            const uint32_t *box, CUtensorMapSwizzle swizzle) {
@@ -109,7 +120,8 @@ bool valid_sink(sattn_sink_mode m, const float *sinks) {
     if (m != SATTN_SINK_KEY0_BIAS && m != SATTN_SINK_NULL_LOGIT) return false;
     return sinks != nullptr;
 }
-bool finite_scale(float s) { return s == s && s - s == 0.0f; }
+// The softmax scale must be finite and positive.
+bool finite_scale(float s) { return s == s && s - s == 0.0f && s > 0.0f; }
 // TMA tiles need 16-byte aligned base addresses.
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -196,7 +208,7 @@ sattn_status sattn_window_fwd(const void *q, const void *k, const void *v, void 
 
 size_t sattn_sparse_workspace_bytes(int32_t B, int32_t M, int32_t H, int32_t d, int32_t K) {
     if (B <= 0 || M <= 0 || H <= 0 || d <= 0 || K <= 0) return 0;
-    return 0;
+    return sparse_tc_workspace_bytes(B, M, H, d, K);
 }
 
 sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t *topk_idxs,
@@ -221,6 +233,10 @@ sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t
                  (int)sink_mode, scale, o, lse, B, M, H, d, N, K, workspace, workspace_bytes,
                  (int)dtype};
     cudaStream_t s = as_stream(cuda_stream);
+    if (dtype == SATTN_BF16) {
+        if (!aligned16(q) || !aligned16(kv_cache)) return SATTN_ERR_INVALID_ARG;
+        return finish(launch_sparse_tc(a, *dev, s), s);
+    }
     return finish(launch_sparse_simt(a, *dev, s), s);
 }
 

@@ -7,23 +7,38 @@
 //    notes that visiting every block and masking costs O(seq_len^2));
 //  * one KV chunk of block-sparse causal attention ("XAttention Offload
 //    Stream Synchronization Fix": per-chunk partial stats, merged later);
-//    the key tiles are the selected 128-key blocks of the chunk.
+//    the key tiles are the two 64-key halves of each selected 128-key block.
 //
 // A work item is (128-query tile, query head). A persistent grid of one CTA
-// per SM walks the items; each CTA has three roles:
-//   warp 0        TMA producer: Q tile (double-buffered), K and V tiles
-//                 (two stages each), 128B-swizzled, K-major rows of 256 B.
-//   warp 1        MMA issuer (one thread): S = Q K^T into TMEM (two S
-//                 buffers), then O += P V into TMEM (two O buffers).
-//   warps 2..5    softmax + epilogue: thread = query row = TMEM lane. Each
-//                 row keeps its running max m and sum l in the log2 domain;
-//                 P (bf16) goes to shared memory as the A operand of P V.
+// per SM (kernels that allocate tensor memory run one CTA per SM) walks the
+// items with two independent pipeline slots, each with its own shared
+// memory, barriers, 256 TMEM columns and item stream. Per slot:
+//   warp 2s       TMA producer: the Q tile, then K and V tiles of 64 keys
+//                 (two stages each), 128B-swizzled, rows of 256 B.
+//   warp 2s+1     MMA issuer (one thread): S = Q K^T into TMEM (64
+//                 columns), then O += P V into TMEM with P read from TMEM
+//                 (A operand in tensor memory, two P buffers of 32 columns).
+//   warps 4+4s..  softmax + epilogue (four warps): thread = query row = TMEM lane. Each
+//                 row keeps its running max m and sum l in the log2 domain.
+// S of tile j+1 is computed as soon as the softmax has loaded S of tile j.
+// No tensor-memory column is read by one MMA and written by a later one, so
+// ordering rests only on commits and barriers; since S of tile j is issued
+// after P V of tile j-2, seeing S(j) complete also frees P buffer j % 2.
+// The two slots give every SM sub-partition two softmax warps and let one
+// slot's MMAs overlap the other's softmax.
+//
+// Softmax per tile: the maximum is taken over the raw scores (the scale is
+// positive), and each probability is ex2(s * scale*log2(e) - m) with the
+// multiply-add done two lanes at a time (f32x2). Chunks of 32 keys that no
+// row of a warp can see are skipped; chunks every row sees are not masked.
 // The running max is only moved when a tile raises it by more than 2^8, so
-// the accumulator in TMEM is rarely rescaled (P <= 256 otherwise, exact in
-// fp32 sums). Null-logit sinks start from m = sink, l = 1; key-0 sinks add
-// the sink to key 0's logit where it is visible.
+// the accumulator in TMEM is rarely rescaled (P <= 256 otherwise).
+// Null-logit sinks start from m = sink, l = 1; key-0 sinks add the sink to
+// key 0's logit where it is visible.
 #include <limits.h>
 #include <math.h>
+#include <stddef.h>
+#include <stdio.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -31,19 +46,28 @@
 namespace sattn {
 namespace {
 
-constexpr int BM = 128;                  // queries per tile (TMEM lanes)
-constexpr int BN = 128;                  // keys per tile
-constexpr int HD = 128;                  // head dim
-constexpr uint32_t TILE = BM * HD * 2;   // bytes of one bf16 128x128 tile
-constexpr uint32_t HALF = TILE / 2;      // one 64-column (128-byte) swizzled half
-constexpr int NTHREADS = 192;
-constexpr float TAU = 8.0f;              // rescale threshold (log2 units)
+constexpr int BM = 128;                   // queries per tile (TMEM lanes)
+constexpr int BN = 64;                    // keys per tile
+constexpr int HD = 128;                   // head dim
+constexpr uint32_t Q_TILE = BM * HD * 2;  // 32 KB
+constexpr uint32_t Q_HALF = Q_TILE / 2;   // 64 columns of d (128-byte rows)
+constexpr uint32_t KV_TILE = BN * HD * 2; // 16 KB
+constexpr uint32_t KV_HALF = KV_TILE / 2;
+constexpr int NSLOTS = 2;
+constexpr int NTHREADS = 128 * (NSLOTS + 1);  // 2 role warps + 4 softmax warps per slot
+constexpr uint32_t SLOT_COLS = 256;       // per slot: S (64) + P[2] (32 each) + O (128)
+constexpr uint32_t S_COL = 0, P_COL = 64;
+constexpr uint32_t TMEM_COLS = SLOT_COLS * NSLOTS;
+constexpr uint32_t O_COL = 128;
+constexpr float TAU = 8.0f;               // rescale threshold (log2 units)
+constexpr unsigned FULL = 0xffffffffu;
 
 enum : int { MODE_WINDOW = 0, MODE_BLOCK = 1 };
 
 struct TcParams {
     int H, Hkv, groups, num_items;
-    float scale_l2;  // scale * log2(e)
+    float scale_l2;  // scale * log2(e) (> 0)
+    float inv_scale; // 1 / scale
     // window
     const int32_t *cu_seqlens;
     int num_seqs, T, tiles_per_seq, wl, wr, causal;
@@ -57,18 +81,30 @@ struct TcParams {
     float *o_part, *lse_part;
 };
 
-struct __align__(1024) Smem {
-    uint8_t q[2][TILE];
-    uint8_t k[2][TILE];
-    uint8_t v[2][TILE];
-    uint8_t p[TILE];
+struct Bars {
+    uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
+    // p_full is per P buffer: a softmax warp may run one tile ahead of the
+    // others, so arrivals for consecutive tiles must not share a barrier.
+    uint64_t s_full, s_empty, p_full[2], pv_done, o_full, o_empty, drain;
 };
 
-struct Bars {
-    uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
-    uint64_t s_full[2], s_empty[2], p_full, p_empty, o_full[2], o_empty[2], drain;
+// Operand tiles of one pipeline slot (96 KB).
+struct Slot {
+    uint8_t q[Q_TILE];
+    uint8_t k[2][KV_TILE];
+    uint8_t v[2][KV_TILE];
+};
+static_assert(offsetof(Slot, k) % 1024 == 0 && offsetof(Slot, v) % 1024 == 0 &&
+                  sizeof(Slot) % 1024 == 0,
+              "operand tiles must sit on 1024-byte boundaries");
+
+// The whole shared-memory footprint (dynamic only; the base of the CTA's
+// shared window is 1024-byte aligned, as the 128B swizzle needs).
+struct Smem {
+    Slot slot[NSLOTS];
+    Bars bars[NSLOTS];
     uint32_t tmem_base;
-    int abort;
+    int abort;  // any role that gives up stops every role of the CTA
 };
 
 struct Item {
@@ -80,7 +116,7 @@ struct Item {
     int qpos0;     // window: local index of query row 0; block: absolute position
     int lo, hi, L; // window: key band of the tile (local), sequence length
     const uint8_t *mrow;
-    int kb_lo, kb_hi;
+    int kb_lo, kb_hi, kend;  // block: 128-key block range, key limit
 };
 
 template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &p, int v) {
@@ -121,11 +157,19 @@ template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &
         it.qpos0 = p.q_pos0 + qs;
         int end = p.kv_end;
         if (p.causal) end = min(end, it.qpos0 + it.nq);
-        it.kb_lo = p.kv_begin / BN;
-        it.kb_hi = end > p.kv_begin ? (end - 1) / BN : it.kb_lo - 1;
+        it.kend = end;
+        it.kb_lo = p.kv_begin / 128;
+        it.kb_hi = end > p.kv_begin ? (end - 1) / 128 : it.kb_lo - 1;
         it.mrow = p.mask + ((size_t)it.h * p.QB + qb) * p.KB;
         int n = 0;
-        for (int kb = it.kb_lo; kb <= it.kb_hi; ++kb) n += __ldg(it.mrow + kb) != 0;
+        for (int kb = it.kb_lo; kb <= it.kb_hi; ++kb) {
+            if (!__ldg(it.mrow + kb)) continue;
+            // 64-key halves that overlap [kv_begin, end)
+            for (int hh = 0; hh < 2; ++hh) {
+                const int base = kb * 128 + hh * BN;
+                n += (base < end && base + BN > p.kv_begin) ? 1 : 0;
+            }
+        }
         it.ntiles = n;
         it.valid = true;
     }
@@ -134,79 +178,89 @@ template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &
 
 // Key coordinate of the first key of each successive tile of an item.
 template <int MODE> struct TileIter {
-    int j, kb;
-    __device__ explicit TileIter(const Item &it) : j(0), kb(it.kb_lo - 1) {}
-    __device__ int next(const Item &it) {
+    int j, kb, hh;
+    __device__ explicit TileIter(const Item &it) : j(0), kb(it.kb_lo - 1), hh(1) {}
+    __device__ int next(const TcParams &p, const Item &it) {
         if (MODE == MODE_WINDOW) return it.lo + BN * (j++);
-        do { ++kb; } while (kb <= it.kb_hi && __ldg(it.mrow + kb) == 0);
-        ++j;
-        return kb * BN;
+        for (;;) {
+            if (kb > it.kb_hi) return it.kb_hi * 128;  // unreachable for a fixed mask
+            if (hh == 1) {
+                do { ++kb; } while (kb <= it.kb_hi && __ldg(it.mrow + kb) == 0);
+                hh = 0;
+            } else {
+                hh = 1;
+            }
+            const int base = kb * 128 + hh * BN;
+            if (base < it.kend && base + BN > p.kv_begin) {
+                ++j;
+                return base;
+            }
+        }
     }
 };
 
-// K-major operand (rows of 128 B, two 64-column halves HALF bytes apart):
-// descriptor for the kk-th 16-element K slice.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk) {
-    return smem_desc_sw128(base + (uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u, 16u,
+// K-major operand with 128-byte rows split in 64-column halves `half` bytes
+// apart: descriptor for the kk-th 16-element K slice.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk, uint32_t half) {
+    return smem_desc_sw128(base + (uint32_t)(kk >> 2) * half + (uint32_t)(kk & 3) * 32u, 16u,
                            1024u);
 }
-// MN-major operand (V: rows = keys, 64-column halves of d HALF bytes apart):
+// MN-major operand (V: rows = keys, 64-column halves of d KV_HALF bytes apart):
 // descriptor for the kk-th 16-key slice.
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
-    return smem_desc_sw128(base + (uint32_t)kk * 2048u, HALF, 1024u);
+    return smem_desc_sw128(base + (uint32_t)kk * 2048u, KV_HALF, 1024u);
 }
 
-constexpr uint32_t IDESC_S = idesc_bf16_f32(128, 128, 0, 0);
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, 128, 0, 1);
+constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HD, 0, 1);
 
 // ------------------------------------------------------------------ producer
 
 template <int MODE>
 __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtensorMap *tk,
-                         const CUtensorMap *tv, Smem &sm, Bars &b, const DevCtx &ctx) {
+                         const CUtensorMap *tv, Slot &sm, Bars &b, volatile int *abort,
+                         int first, int stride, const DevCtx &ctx) {
     prefetch_tmap(tq);
     prefetch_tmap(tk);
     prefetch_tmap(tv);
     int qi = 0, kt = 0;
     bool ok = true;
-    for (int v = blockIdx.x; ok && v < p.num_items; v += gridDim.x) {
+    for (int v = first; ok && v < p.num_items; v += stride) {
         const Item it = decode_item<MODE>(p, v);
         if (!it.valid || it.ntiles == 0) continue;
-        const int qb = qi & 1;
-        if (qi >= 2) ok = mbar_wait(smem_u32(&b.q_empty[qb]), ((qi >> 1) - 1) & 1, ctx, &b.abort);
+        if (qi >= 1) ok = mbar_wait(smem_u32(&b.q_empty), (qi - 1) & 1, ctx, abort);
         if (!ok) break;
-        const uint32_t qbar = smem_u32(&b.q_full[qb]);
-        mbar_arrive_expect_tx(qbar, TILE);
-        tma_load_3d(smem_u32(sm.q[qb]), tq, qbar, 0, it.h, it.q_row0);
-        tma_load_3d(smem_u32(sm.q[qb]) + HALF, tq, qbar, 64, it.h, it.q_row0);
+        const uint32_t qbar = smem_u32(&b.q_full);
+        mbar_arrive_expect_tx(qbar, Q_TILE);
+        tma_load_3d(smem_u32(sm.q), tq, qbar, 0, it.h, it.q_row0);
+        tma_load_3d(smem_u32(sm.q) + Q_HALF, tq, qbar, 64, it.h, it.q_row0);
         ++qi;
         TileIter<MODE> ti(it);
         for (int j = 0; j < it.ntiles; ++j, ++kt) {
-            const int row = it.key_row0 + ti.next(it);
+            const int row = it.key_row0 + ti.next(p, it);
             const int st = kt & 1, use = kt >> 1;
-            if (use >= 1) ok = mbar_wait(smem_u32(&b.k_empty[st]), (use - 1) & 1, ctx, &b.abort);
+            if (use >= 1) ok = mbar_wait(smem_u32(&b.k_empty[st]), (use - 1) & 1, ctx, abort);
             if (!ok) break;
             const uint32_t kbar = smem_u32(&b.k_full[st]);
-            mbar_arrive_expect_tx(kbar, TILE);
+            mbar_arrive_expect_tx(kbar, KV_TILE);
             tma_load_3d(smem_u32(sm.k[st]), tk, kbar, 0, it.g, row);
-            tma_load_3d(smem_u32(sm.k[st]) + HALF, tk, kbar, 64, it.g, row);
-            if (use >= 1) ok = mbar_wait(smem_u32(&b.v_empty[st]), (use - 1) & 1, ctx, &b.abort);
+            tma_load_3d(smem_u32(sm.k[st]) + KV_HALF, tk, kbar, 64, it.g, row);
+            if (use >= 1) ok = mbar_wait(smem_u32(&b.v_empty[st]), (use - 1) & 1, ctx, abort);
             if (!ok) break;
             const uint32_t vbar = smem_u32(&b.v_full[st]);
-            mbar_arrive_expect_tx(vbar, TILE);
+            mbar_arrive_expect_tx(vbar, KV_TILE);
             tma_load_3d(smem_u32(sm.v[st]), tv, vbar, 0, it.g, row);
-            tma_load_3d(smem_u32(sm.v[st]) + HALF, tv, vbar, 64, it.g, row);
+            tma_load_3d(smem_u32(sm.v[st]) + KV_HALF, tv, vbar, 64, it.g, row);
         }
     }
     if (!ok) {
         // Let copies already in flight land before the CTA leaves (bounded).
-        DevCtx c2 = ctx;
         int zero = 0;
+        if (qi > 0) mbar_wait(smem_u32(&b.q_full), (qi - 1) & 1, ctx, &zero);
         for (int i = 0; i < 2; ++i) {
-            if (qi > i) mbar_wait(smem_u32(&b.q_full[(qi - 1 - i) & 1]), ((qi - 1 - i) >> 1) & 1, c2, &zero);
             if (kt > i) {
-                mbar_wait(smem_u32(&b.k_full[(kt - 1 - i) & 1]), ((kt - 1 - i) >> 1) & 1, c2, &zero);
-                mbar_wait(smem_u32(&b.v_full[(kt - 1 - i) & 1]), ((kt - 1 - i) >> 1) & 1, c2, &zero);
+                mbar_wait(smem_u32(&b.k_full[(kt - 1 - i) & 1]), ((kt - 1 - i) >> 1) & 1, ctx, &zero);
+                mbar_wait(smem_u32(&b.v_full[(kt - 1 - i) & 1]), ((kt - 1 - i) >> 1) & 1, ctx, &zero);
             }
         }
     }
@@ -215,58 +269,57 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
 // ------------------------------------------------------------------ MMA issuer
 
 template <int MODE>
-__device__ void mma_issuer(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem, const DevCtx &ctx) {
-    int qi = 0, kt = 0, sc = 0, pc = 0, oc = 0;
+__device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *abort,
+                           uint32_t tmem, int first, int stride, const DevCtx &ctx) {
+    int qi = 0, kt = 0, pc = 0;
     bool ok = true;
-    const uint32_t p_base = smem_u32(sm.p);
-    for (int v = blockIdx.x; ok && v < p.num_items; v += gridDim.x) {
+    const uint32_t q_base = smem_u32(sm.q);
+    const uint32_t o_tmem = tmem + O_COL;
+    for (int v = first; ok && v < p.num_items; v += stride) {
         const Item it = decode_item<MODE>(p, v);
         if (!it.valid || it.ntiles == 0) continue;
-        const int qb = qi & 1, ob = oc & 1;
-        const uint32_t q_base = smem_u32(sm.q[qb]);
-        const uint32_t o_tmem = tmem + 256u + (uint32_t)ob * 128u;
-        ok = mbar_wait(smem_u32(&b.q_full[qb]), (qi >> 1) & 1, ctx, &b.abort);
+        ok = mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort);
         const int n = it.ntiles, kt0 = kt;
         auto issue_pv = [&](int jj) -> bool {
             const int st = (kt0 + jj) & 1, use = (kt0 + jj) >> 1;
-            if (!mbar_wait(smem_u32(&b.p_full), pc & 1, ctx, &b.abort)) return false;
-            if (!mbar_wait(smem_u32(&b.v_full[st]), use & 1, ctx, &b.abort)) return false;
-            if (jj == 0 && oc >= 2 &&
-                !mbar_wait(smem_u32(&b.o_empty[ob]), ((oc >> 1) - 1) & 1, ctx, &b.abort))
+            if (!mbar_wait(smem_u32(&b.p_full[pc & 1]), (pc >> 1) & 1, ctx, abort)) return false;
+            if (!mbar_wait(smem_u32(&b.v_full[st]), use & 1, ctx, abort)) return false;
+            if (jj == 0 && qi >= 1 &&
+                !mbar_wait(smem_u32(&b.o_empty), (qi - 1) & 1, ctx, abort))
                 return false;
             tc_fence_after();
             const uint32_t v_base = smem_u32(sm.v[st]);
+            const uint32_t p_tmem = tmem + P_COL + 32u * (uint32_t)(pc & 1);
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-                tc_mma_f16(o_tmem, desc_kmajor(p_base, kk), desc_mnmajor(v_base, kk), IDESC_PV,
-                           (jj > 0 || kk > 0) ? 1u : 0u);
+                tc_mma_f16_ts(o_tmem, p_tmem + 8u * kk, desc_mnmajor(v_base, kk), IDESC_PV,
+                              (jj > 0 || kk > 0) ? 1u : 0u);
             tc_commit(smem_u32(&b.v_empty[st]));
-            tc_commit(smem_u32(&b.p_empty));
+            tc_commit(smem_u32(&b.pv_done));
             ++pc;
             return true;
         };
         for (int j = 0; ok && j < n; ++j) {
-            const int st = (kt0 + j) & 1, use = (kt0 + j) >> 1, sb = sc & 1;
-            if (sc >= 2) ok = mbar_wait(smem_u32(&b.s_empty[sb]), ((sc >> 1) - 1) & 1, ctx, &b.abort);
-            if (ok) ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, &b.abort);
+            // one S buffer: tile t may start once the softmax has loaded tile t-1
+            const int t = kt0 + j, st = t & 1, use = t >> 1;
+            if (t >= 1) ok = mbar_wait(smem_u32(&b.s_empty), (t - 1) & 1, ctx, abort);
+            if (ok) ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort);
             if (!ok) break;
             tc_fence_after();
             const uint32_t k_base = smem_u32(sm.k[st]);
-            const uint32_t s_tmem = tmem + (uint32_t)sb * 128u;
+            const uint32_t s_tmem = tmem + S_COL;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
-                tc_mma_f16(s_tmem, desc_kmajor(q_base, kk), desc_kmajor(k_base, kk), IDESC_S,
-                           kk > 0 ? 1u : 0u);
+                tc_mma_f16(s_tmem, desc_kmajor(q_base, kk, Q_HALF), desc_kmajor(k_base, kk, KV_HALF),
+                           IDESC_S, kk > 0 ? 1u : 0u);
             tc_commit(smem_u32(&b.k_empty[st]));
-            tc_commit(smem_u32(&b.s_full[sb]));
-            if (j == n - 1) tc_commit(smem_u32(&b.q_empty[qb]));
-            ++sc;
+            tc_commit(smem_u32(&b.s_full));
+            if (j == n - 1) tc_commit(smem_u32(&b.q_empty));
             if (j >= 1) ok = issue_pv(j - 1);
         }
         if (ok) ok = issue_pv(n - 1);
-        if (ok) tc_commit(smem_u32(&b.o_full[ob]));
+        if (ok) tc_commit(smem_u32(&b.o_full));
         ++qi;
-        ++oc;
         kt += n;
     }
     // Every tcgen05 operation issued above completes before TMEM is released.
@@ -275,23 +328,49 @@ __device__ void mma_issuer(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem, 
     mbar_wait(smem_u32(&b.drain), 0, ctx, &zero);
 }
 
+// ------------------------------------------------------------------ softmax helpers
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// (a.lo * b.lo + c.lo, a.hi * b.hi + c.hi)
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // ------------------------------------------------------------------ softmax / epilogue
 
 template <int MODE>
-__device__ void softmax_role(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem,
-                             const DevCtx &ctx) {
+__device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, uint32_t tmem,
+                             int first, int stride, const DevCtx &ctx) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t p_base = smem_u32(sm.p);
-    const unsigned FULL = 0xffffffffu;
-    int sc = 0, pc = 0, oc = 0;
+    const uint32_t o_tmem = tmem + O_COL + lane_off;
+    int sc = 0, pc = 0, qi = 0;  // sc: tiles seen, pc: P tiles written
     bool ok = true;
-    for (int v = blockIdx.x; ok && v < p.num_items; v += gridDim.x) {
+    for (int v = first; ok && v < p.num_items; v += stride) {
         const Item it = decode_item<MODE>(p, v);
         if (!it.valid) {
-            if (it.seq_err && warp == 2 && lane == 0) record_error(ctx, DEVERR_SEQLENS);
+            if (it.seq_err && quarter == 0 && lane == 0) record_error(ctx, DEVERR_SEQLENS);
             continue;
         }
         const bool row_valid = r < it.nq;
@@ -305,9 +384,11 @@ __device__ void softmax_role(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem
             }
             continue;
         }
+        const bool warp_all_valid = __all_sync(FULL, row_valid);
         // visible key interval of this row (window: fixed for the item)
         const int qi_loc = it.qpos0 + r;
-        int lo_r = INT_MAX, hi_r = INT_MIN;
+        constexpr int NONE_LO = 1 << 30, NONE_HI = -(1 << 30);  // empty interval
+        int lo_r = NONE_LO, hi_r = NONE_HI;
         if (MODE == MODE_WINDOW && row_valid) {
             lo_r = p.wl < 0 ? 0 : max(0, qi_loc - p.wl);
             hi_r = p.wr < 0 ? it.L - 1 : min(it.L - 1, qi_loc + p.wr);
@@ -315,59 +396,66 @@ __device__ void softmax_role(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem
         }
         const bool null_sink = MODE == MODE_WINDOW && p.sink_mode == 2;
         const bool key0 = MODE == MODE_WINDOW && p.sink_mode == 1;
-        const float sink_l2 = (MODE == MODE_WINDOW && p.sinks) ? __ldg(p.sinks + it.h) * LOG2E : 0.f;
-        float m_run = null_sink ? sink_l2 : -INFINITY;
+        const float sink = (MODE == MODE_WINDOW && p.sinks) ? __ldg(p.sinks + it.h) : 0.f;
+        float m_run = null_sink ? sink * LOG2E : -INFINITY;
         float l = null_sink ? 1.0f : 0.0f;
-        const int ob = oc & 1;
-        const uint32_t o_tmem = tmem + 256u + (uint32_t)ob * 128u + lane_off;
+        const uint64_t scale2 = f2_pack(p.scale_l2, p.scale_l2);
         TileIter<MODE> ti(it);
         for (int j = 0; j < it.ntiles; ++j) {
-            const int base = ti.next(it);
+            const int base = ti.next(p, it);
             if (MODE == MODE_BLOCK) {
                 if (row_valid) {
                     lo_r = max(base, p.kv_begin);
                     hi_r = min(base + BN - 1, p.kv_end - 1);
                     if (p.causal) hi_r = min(hi_r, qi_loc);
                 } else {
-                    lo_r = INT_MAX;
-                    hi_r = INT_MIN;
+                    lo_r = NONE_LO;
+                    hi_r = NONE_HI;
                 }
             }
+            // warp-level: union of the rows' intervals (for skipping) and
+            // their intersection (chunks inside it need no masking)
             const int wlo = __reduce_min_sync(FULL, lo_r);
             const int whi = __reduce_max_sync(FULL, hi_r);
-            const int sb = sc & 1;
-            if (!mbar_wait(smem_u32(&b.s_full[sb]), (sc >> 1) & 1, ctx, &b.abort)) { ok = false; break; }
+            const int ilo = __reduce_max_sync(FULL, row_valid ? lo_r : INT_MIN);
+            const int ihi = __reduce_min_sync(FULL, row_valid ? hi_r : INT_MAX);
+            if (!mbar_wait(smem_u32(&b.s_full), sc & 1, ctx, abort)) { ok = false; break; }
             tc_fence_after();
-            uint32_t x[4][32];
-            unsigned live = 0;
+            uint32_t x[2][32];
+            unsigned live = 0, full = 0;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 const int k0 = base + 32 * c;
                 if (!(k0 + 31 < wlo || k0 > whi)) {
                     live |= 1u << c;
-                    tmem_ld32(tmem + (uint32_t)sb * 128u + 32u * c + lane_off, x[c]);
+                    if (warp_all_valid && k0 >= ilo && k0 + 31 <= ihi) full |= 1u << c;
+                    tmem_ld32(tmem + S_COL + 32u * c + lane_off, x[c]);
                 }
             }
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&b.s_empty[sb]));
+            if (lane == 0) mbar_arrive(smem_u32(&b.s_empty));
             ++sc;
-            // scale, mask, sink bias; tile maximum
-            float mt = -INFINITY;
+            // key-0 bias, in raw score units, on the sequence's first key
+            if (key0 && base == 0 && (live & 1u))
+                x[0][0] = __float_as_uint(__uint_as_float(x[0][0]) + sink * p.inv_scale);
+            // mask partial chunks; maximum of the raw scores
+            float mraw = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 if (!(live >> c & 1u)) continue;
+                if (!(full >> c & 1u)) {
+                    const int a = lo_r - (base + 32 * c), z = hi_r - (base + 32 * c);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int key = base + 32 * c + e;
-                    float s = __uint_as_float(x[c][e]) * p.scale_l2;
-                    if (key0 && key == 0) s += sink_l2;
-                    s = (key >= lo_r && key <= hi_r) ? s : -INFINITY;
-                    x[c][e] = __float_as_uint(s);
-                    mt = fmaxf(mt, s);
+                    for (int e = 0; e < 32; ++e)
+                        if (e < a || e > z) x[c][e] = __float_as_uint(-INFINITY);
                 }
+#pragma unroll
+                for (int e = 0; e < 32; e += 2)
+                    mraw = max3(mraw, __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
             }
+            const float mt = mraw * p.scale_l2;
             const bool upd = mt > m_run + TAU;
             float alpha = 1.0f;
             if (upd) {
@@ -375,12 +463,14 @@ __device__ void softmax_role(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem
                 l *= alpha;
                 m_run = mt;
             }
-            // P buffer free == previous P V finished (also makes O stable)
-            if (pc >= 1 && !mbar_wait(smem_u32(&b.p_empty), (pc - 1) & 1, ctx, &b.abort)) {
-                ok = false;
-                break;
-            }
             if (j >= 1 && __any_sync(FULL, upd)) {
+                // O is rescaled in place: the previous P V must have finished.
+                // (S of this tile complete implies the P V before that one has,
+                // so this parity wait cannot alias.)
+                if (!mbar_wait(smem_u32(&b.pv_done), (pc - 1) & 1, ctx, abort)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -395,44 +485,44 @@ __device__ void softmax_role(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem
                 tc_wait_st();
             }
             const float mu = (m_run == -INFINITY) ? 0.0f : m_run;
+            const uint64_t negm2 = f2_pack(-mu, -mu);
+            uint64_t lsum = f2_pack(0.f, 0.f);
+            uint32_t pw[32];  // P as bf16 pairs: word w holds keys 2w (low half) and 2w+1
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t region = p_base + (uint32_t)(c >> 1) * HALF;
+            for (int c = 0; c < 2; ++c) {
                 if (live >> c & 1u) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const float a0 = ex2(__uint_as_float(x[c][8 * u + 2 * e2]) - mu);
-                            const float a1 = ex2(__uint_as_float(x[c][8 * u + 2 * e2 + 1]) - mu);
-                            l += a0 + a1;
-                            w[e2] = pack_bf16x2(a0, a1);
-                        }
-                        const uint32_t addr = region + sw128_offset(r, (c & 1) * 4 + u);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                                     : "memory");
+                    for (int e = 0; e < 32; e += 2) {
+                        const uint64_t arg = f2_fma(
+                            f2_pack(__uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1])),
+                            scale2, negm2);
+                        float a0, a1;
+                        f2_unpack(arg, a0, a1);
+                        a0 = ex2(a0);
+                        a1 = ex2(a1);
+                        lsum = f2_add(lsum, f2_pack(a0, a1));
+                        pw[16 * c + e / 2] = pack_bf16x2(a0, a1);
                     }
                 } else {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint32_t addr = region + sw128_offset(r, (c & 1) * 4 + u);
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr),
-                                     "r"(0u)
-                                     : "memory");
-                    }
+                    for (int e = 0; e < 16; ++e) pw[16 * c + e] = 0u;
                 }
             }
-            fence_proxy_async_smem();
+            {
+                float s0, s1;
+                f2_unpack(lsum, s0, s1);
+                l += s0 + s1;
+            }
+            tmem_st32(tmem + P_COL + 32u * (uint32_t)(pc & 1) + lane_off, pw);
+            tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&b.p_full));
+            if (lane == 0) mbar_arrive(smem_u32(&b.p_full[pc & 1]));
             ++pc;
         }
         if (!ok) break;
         // epilogue: O / l -> global, lse
-        if (!mbar_wait(smem_u32(&b.o_full[ob]), (oc >> 1) & 1, ctx, &b.abort)) { ok = false; break; }
+        if (!mbar_wait(smem_u32(&b.o_full), qi & 1, ctx, abort)) { ok = false; break; }
         tc_fence_after();
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const size_t orow = (size_t)(it.q_row0 + r) * p.H + it.h;
@@ -441,6 +531,11 @@ __device__ void softmax_role(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem
             uint32_t ov[32];
             tmem_ld32(o_tmem + 32u * c, ov);
             tc_wait_ld();
+            if (c == 3) {  // O fully read: the next item's first P V may overwrite it
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
+            }
             if (!row_valid) continue;
             if (MODE == MODE_WINDOW) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * HD + 32 * c);
@@ -469,10 +564,7 @@ __device__ void softmax_role(const TcParams &p, Smem &sm, Bars &b, uint32_t tmem
                 p.lse_part[orow] = lse;
             }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&b.o_empty[ob]));
-        ++oc;
+        ++qi;
     }
 }
 
@@ -480,61 +572,76 @@ template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, const TcParams p, const DevCtx ctx) {
-    extern __shared__ uint8_t dsmem[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(dsmem) + 1023) &
-                                         ~static_cast<uintptr_t>(1023));
-    __shared__ Bars b;
+    extern __shared__ __align__(1024) uint8_t dsmem[];
+    Smem &sm = *reinterpret_cast<Smem *>(dsmem);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The 128B swizzle pattern is anchored to 1024-byte boundaries of the
+    // shared window; the layout above relies on an aligned base.
+    if (smem_u32(dsmem) & 1023u) {
+        if (threadIdx.x == 0) record_error(ctx, DEVERR_LAYOUT);
+        return;
+    }
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&b.q_full[i]), 1);
-            mbar_init(smem_u32(&b.q_empty[i]), 1);
-            mbar_init(smem_u32(&b.k_full[i]), 1);
-            mbar_init(smem_u32(&b.k_empty[i]), 1);
-            mbar_init(smem_u32(&b.v_full[i]), 1);
-            mbar_init(smem_u32(&b.v_empty[i]), 1);
-            mbar_init(smem_u32(&b.s_full[i]), 1);
-            mbar_init(smem_u32(&b.s_empty[i]), 4);
-            mbar_init(smem_u32(&b.o_full[i]), 1);
-            mbar_init(smem_u32(&b.o_empty[i]), 4);
+        for (int s = 0; s < NSLOTS; ++s) {
+            Bars &b = sm.bars[s];
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(smem_u32(&b.k_full[i]), 1);
+                mbar_init(smem_u32(&b.k_empty[i]), 1);
+                mbar_init(smem_u32(&b.v_full[i]), 1);
+                mbar_init(smem_u32(&b.v_empty[i]), 1);
+            }
+            mbar_init(smem_u32(&b.s_full), 1);
+            mbar_init(smem_u32(&b.s_empty), 4);
+            mbar_init(smem_u32(&b.q_full), 1);
+            mbar_init(smem_u32(&b.q_empty), 1);
+            mbar_init(smem_u32(&b.p_full[0]), 4);
+            mbar_init(smem_u32(&b.p_full[1]), 4);
+            mbar_init(smem_u32(&b.pv_done), 1);
+            mbar_init(smem_u32(&b.o_full), 1);
+            mbar_init(smem_u32(&b.o_empty), 4);
+            mbar_init(smem_u32(&b.drain), 1);
         }
-        mbar_init(smem_u32(&b.p_full), 4);
-        mbar_init(smem_u32(&b.p_empty), 1);
-        mbar_init(smem_u32(&b.drain), 1);
-        b.abort = 0;
+        sm.abort = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&b.tmem_base), 512);
+        tmem_alloc(smem_u32(&sm.tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = b.tmem_base;
-    if (warp == 0) {
-        if (lane == 0) producer<MODE>(p, &tq, &tk, &tv, sm, b, ctx);
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) mma_issuer<MODE>(p, sm, b, tmem, ctx);
+    // slot s: warps 2s (producer), 2s+1 (MMA), 4+4s .. 7+4s (softmax)
+    const int slot = warp < 2 * NSLOTS ? warp >> 1 : (warp - 2 * NSLOTS) >> 2;
+    const uint32_t tmem = sm.tmem_base + (uint32_t)slot * SLOT_COLS;
+    const int first = blockIdx.x * NSLOTS + slot, stride = gridDim.x * NSLOTS;
+    if (warp < 2 * NSLOTS) {
+        if (lane == 0) {
+            if ((warp & 1) == 0)
+                producer<MODE>(p, &tq, &tk, &tv, sm.slot[slot], sm.bars[slot], &sm.abort, first,
+                               stride, ctx);
+            else
+                mma_issuer<MODE>(p, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride,
+                                 ctx);
+        }
         __syncwarp();
     } else {
-        softmax_role<MODE>(p, sm, b, tmem, ctx);
+        softmax_role<MODE>(p, sm.bars[slot], &sm.abort, tmem, first, stride, ctx);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(sm.tmem_base, TMEM_COLS);
     }
 }
 
 // ------------------------------------------------------------------ host side
 
-CUresult make_map(CUtensorMap *m, const void *base, int rows, int heads) {
+CUresult make_map(CUtensorMap *m, const void *base, int rows, int heads, uint32_t box_rows) {
     const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)heads, (uint64_t)rows};
     const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)HD * 2 * heads};
-    const uint32_t box[3] = {64, 1, (uint32_t)BM};
+    const uint32_t box[3] = {64, 1, box_rows};
     return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                              strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -545,10 +652,10 @@ template <int MODE> cudaError_t launch(const TcParams &p, const void *q, int q_r
     for (const void *ptr : {q, k, v})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return cudaErrorMisalignedAddress;
     CUtensorMap tq, tk, tv;
-    if (make_map(&tq, q, q_rows, p.H) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (make_map(&tk, k, kv_rows, p.Hkv) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (make_map(&tv, v, kv_rows, p.Hkv) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(Smem) + 1024;
+    if (make_map(&tq, q, q_rows, p.H, BM) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (make_map(&tk, k, kv_rows, p.Hkv, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (make_map(&tv, v, kv_rows, p.Hkv, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(Smem);
     static bool attr_set[64] = {};
     if (!attr_set[dev.device & 63]) {
         cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<MODE>,
@@ -556,8 +663,13 @@ template <int MODE> cudaError_t launch(const TcParams &p, const void *q, int q_r
         if (e != cudaSuccess) return e;
         attr_set[dev.device & 63] = true;
     }
-    const int grid = p.num_items < dev.sm_count ? p.num_items : dev.sm_count;
+    const int streams = (p.num_items + NSLOTS - 1) / NSLOTS;
+    const int grid = streams < dev.sm_count ? streams : dev.sm_count;
     DevCtx ctx{dev.err, wait_limit_ns()};
+    if (verbose())
+        fprintf(stderr, "sattn: attn_tc_kernel<%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",
+                MODE == MODE_WINDOW ? "window" : "block", grid, NTHREADS, smem, NSLOTS,
+                p.num_items);
     attn_tc_kernel<MODE><<<grid, NTHREADS, smem, s>>>(tq, tk, tv, p, ctx);
     return cudaGetLastError();
 }
@@ -570,6 +682,7 @@ cudaError_t launch_window_tc(const WindowArgs &a, const DevInfo &dev, cudaStream
     p.Hkv = a.Hkv;
     p.groups = a.H / a.Hkv;
     p.scale_l2 = a.scale * LOG2E;
+    p.inv_scale = 1.0f / a.scale;
     p.cu_seqlens = a.cu_seqlens;
     p.num_seqs = a.num_seqs;
     p.T = a.T;
@@ -595,6 +708,7 @@ cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t
     p.Hkv = a.Hkv;
     p.groups = a.H / a.Hkv;
     p.scale_l2 = a.scale * LOG2E;
+    p.inv_scale = 1.0f / a.scale;
     p.mask = a.mask;
     p.M = a.M;
     p.Nctx = a.Nctx;
@@ -603,7 +717,7 @@ cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t
     p.kv_end = a.kv_end;
     p.causal = a.causal;
     p.QB = (a.M + BM - 1) / BM;
-    p.KB = (a.Nctx + BN - 1) / BN;
+    p.KB = (a.Nctx + 127) / 128;
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
     const long long items = (long long)p.QB * a.H;

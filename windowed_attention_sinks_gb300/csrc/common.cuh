@@ -18,6 +18,7 @@ namespace sattn {
 constexpr unsigned DEVERR_TIMEOUT = 1u;
 constexpr unsigned DEVERR_INDEX = 2u;    // index entry outside [-1, N)
 constexpr unsigned DEVERR_SEQLENS = 4u;  // malformed cu_seqlens
+constexpr unsigned DEVERR_LAYOUT = 8u;   // shared-memory base not 1024-byte aligned
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -189,6 +190,19 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16. A occupies 128 lanes, two
+// bf16 per 32-bit column (the even K index in the low half), 8 columns per
+// 16-element K slice.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 

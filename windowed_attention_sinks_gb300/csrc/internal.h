@@ -21,6 +21,8 @@ struct DevInfo {
 // Per-device facts, initialised once per device (thread-safe).
 const DevInfo *device_info(cudaError_t *e);
 uint64_t wait_limit_ns();
+// True when the environment variable SATTN_VERBOSE is set (launch reports on stderr).
+bool verbose();
 
 // cuTensorMapEncodeTiled through the driver entry point (no libcuda link).
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank,
