@@ -116,6 +116,36 @@ sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t
 /* Workspace size (bytes) that lets sattn_sparse_fwd split each index list. */
 size_t sattn_sparse_workspace_bytes(int32_t B, int32_t M, int32_t H, int32_t d, int32_t K);
 
+/* Size in bytes of the scratch array built into the library for
+ * sattn_sparse_fwd_static_scratch. */
+#define SATTN_SPARSE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * sattn_sparse_fwd for callers that cannot allocate device memory. (The pages
+ * have no counterpart to this call; it exists for such callers: a plug-in
+ * whose host application owns all device memory, a loop whose policy forbids
+ * cudaMalloc/cudaFree after start-up, or C code given only tensor pointers
+ * and a stream.)
+ *
+ * Same arguments and results as sattn_sparse_fwd without the workspace: the
+ * partial results of a split index list go to a fixed array of
+ * SATTN_SPARSE_STATIC_SCRATCH_BYTES compiled into the library, which every GPU
+ * that loads the library holds until the process exits. Nothing is allocated.
+ * A call whose sattn_sparse_workspace_bytes(B, M, H, d, K) exceeds that size
+ * is rejected with SATTN_ERR_INVALID_ARG before anything runs.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture. All calls share the array and it keeps the last call's contents
+ * (nothing in it needs to start at zero); calls whose work overlaps on the GPU
+ * race on it, so issue them on one stream.
+ */
+sattn_status sattn_sparse_fwd_static_scratch(const void *q, const void *kv_cache,
+                                             const int32_t *topk_idxs, const float *sinks,
+                                             sattn_sink_mode sink_mode, float scale, void *o,
+                                             float *lse, int32_t B, int32_t M, int32_t H,
+                                             int32_t d, int32_t N, int32_t K, sattn_dtype dtype,
+                                             void *cuda_stream);
+
 /*
  * Merge of chunk partials through their log-sum-exp ("XAttention Offload
  * Stream Synchronization Fix", technical details: partial (m_i, l_i) stats per
