@@ -18,7 +18,8 @@ F32, BF16 = 0, 1
 BLOCK = 128
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libsattn.so")
+# SATTN_LIBRARY may name another build of libsattn.so to load instead.
+LIB_PATH = os.environ.get("SATTN_LIBRARY") or os.path.join(_PKG, "libsattn.so")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
           4: "device check failed", 5: "device wait timed out"}

@@ -54,6 +54,8 @@ constexpr uint32_t Q_HALF = Q_TILE / 2;   // 64 columns of d (128-byte rows)
 constexpr uint32_t KV_TILE = BN * HD * 2; // 16 KB
 constexpr uint32_t KV_HALF = KV_TILE / 2;
 constexpr int NSLOTS = 2;
+constexpr int KSTAGES = 2;                // K tiles in flight per slot
+constexpr int VSTAGES = 2;                // V tiles in flight per slot
 constexpr int NTHREADS = 128 * (NSLOTS + 1);  // 2 role warps + 4 softmax warps per slot
 constexpr uint32_t SLOT_COLS = 256;       // per slot: S (64) + P[2] (32 each) + O (128)
 constexpr uint32_t S_COL = 0, P_COL = 64;
@@ -82,7 +84,7 @@ struct TcParams {
 };
 
 struct Bars {
-    uint64_t q_full, q_empty, k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t q_full, q_empty, k_full[KSTAGES], k_empty[KSTAGES], v_full[VSTAGES], v_empty[VSTAGES];
     // p_full is per P buffer: a softmax warp may run one tile ahead of the
     // others, so arrivals for consecutive tiles must not share a barrier.
     uint64_t s_full, s_empty, p_full[2], pv_done, o_full, o_empty, drain;
@@ -91,8 +93,8 @@ struct Bars {
 // Operand tiles of one pipeline slot (96 KB).
 struct Slot {
     uint8_t q[Q_TILE];
-    uint8_t k[2][KV_TILE];
-    uint8_t v[2][KV_TILE];
+    uint8_t k[KSTAGES][KV_TILE];
+    uint8_t v[VSTAGES][KV_TILE];
 };
 static_assert(offsetof(Slot, k) % 1024 == 0 && offsetof(Slot, v) % 1024 == 0 &&
                   sizeof(Slot) % 1024 == 0,
@@ -223,7 +225,32 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
     prefetch_tmap(tq);
     prefetch_tmap(tk);
     prefetch_tmap(tv);
-    int qi = 0, kt = 0;
+    // Loads are issued in the order their stages free up: S of tile t frees
+    // K stage t, P V of tile t frees V stage t, and the MMA issues S(t+1)
+    // before P V(t), so V runs one tile behind K.
+    int qi = 0, kt = 0, vt = 0;
+    auto load_k = [&](const Item &it, int row) -> bool {
+        const int st = kt % KSTAGES, use = kt / KSTAGES;
+        if (use >= 1 && !mbar_wait(smem_u32(&b.k_empty[st]), (use - 1) & 1, ctx, abort))
+            return false;
+        const uint32_t bar = smem_u32(&b.k_full[st]);
+        mbar_arrive_expect_tx(bar, KV_TILE);
+        tma_load_3d(smem_u32(sm.k[st]), tk, bar, 0, it.g, row);
+        tma_load_3d(smem_u32(sm.k[st]) + KV_HALF, tk, bar, 64, it.g, row);
+        ++kt;
+        return true;
+    };
+    auto load_v = [&](int g, int row) -> bool {
+        const int st = vt % VSTAGES, use = vt / VSTAGES;
+        if (use >= 1 && !mbar_wait(smem_u32(&b.v_empty[st]), (use - 1) & 1, ctx, abort))
+            return false;
+        const uint32_t bar = smem_u32(&b.v_full[st]);
+        mbar_arrive_expect_tx(bar, KV_TILE);
+        tma_load_3d(smem_u32(sm.v[st]), tv, bar, 0, g, row);
+        tma_load_3d(smem_u32(sm.v[st]) + KV_HALF, tv, bar, 64, g, row);
+        ++vt;
+        return true;
+    };
     bool ok = true;
     for (int v = first; ok && v < p.num_items; v += stride) {
         const Item it = decode_item<MODE>(p, v);
@@ -236,33 +263,23 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
         tma_load_3d(smem_u32(sm.q) + Q_HALF, tq, qbar, 64, it.h, it.q_row0);
         ++qi;
         TileIter<MODE> ti(it);
-        for (int j = 0; j < it.ntiles; ++j, ++kt) {
+        int prev_row = 0;
+        for (int j = 0; j < it.ntiles; ++j) {
             const int row = it.key_row0 + ti.next(p, it);
-            const int st = kt & 1, use = kt >> 1;
-            if (use >= 1) ok = mbar_wait(smem_u32(&b.k_empty[st]), (use - 1) & 1, ctx, abort);
-            if (!ok) break;
-            const uint32_t kbar = smem_u32(&b.k_full[st]);
-            mbar_arrive_expect_tx(kbar, KV_TILE);
-            tma_load_3d(smem_u32(sm.k[st]), tk, kbar, 0, it.g, row);
-            tma_load_3d(smem_u32(sm.k[st]) + KV_HALF, tk, kbar, 64, it.g, row);
-            if (use >= 1) ok = mbar_wait(smem_u32(&b.v_empty[st]), (use - 1) & 1, ctx, abort);
-            if (!ok) break;
-            const uint32_t vbar = smem_u32(&b.v_full[st]);
-            mbar_arrive_expect_tx(vbar, KV_TILE);
-            tma_load_3d(smem_u32(sm.v[st]), tv, vbar, 0, it.g, row);
-            tma_load_3d(smem_u32(sm.v[st]) + KV_HALF, tv, vbar, 64, it.g, row);
+            if (!(ok = load_k(it, row))) break;
+            if (j >= 1 && !(ok = load_v(it.g, prev_row))) break;
+            prev_row = row;
         }
+        if (ok) ok = load_v(it.g, prev_row);
     }
     if (!ok) {
         // Let copies already in flight land before the CTA leaves (bounded).
         int zero = 0;
         if (qi > 0) mbar_wait(smem_u32(&b.q_full), (qi - 1) & 1, ctx, &zero);
-        for (int i = 0; i < 2; ++i) {
-            if (kt > i) {
-                mbar_wait(smem_u32(&b.k_full[(kt - 1 - i) & 1]), ((kt - 1 - i) >> 1) & 1, ctx, &zero);
-                mbar_wait(smem_u32(&b.v_full[(kt - 1 - i) & 1]), ((kt - 1 - i) >> 1) & 1, ctx, &zero);
-            }
-        }
+        for (int i = 1; i <= KSTAGES && i <= kt; ++i)
+            mbar_wait(smem_u32(&b.k_full[(kt - i) % KSTAGES]), ((kt - i) / KSTAGES) & 1, ctx, &zero);
+        for (int i = 1; i <= VSTAGES && i <= vt; ++i)
+            mbar_wait(smem_u32(&b.v_full[(vt - i) % VSTAGES]), ((vt - i) / VSTAGES) & 1, ctx, &zero);
     }
 }
 
@@ -281,7 +298,7 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
         ok = mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort);
         const int n = it.ntiles, kt0 = kt;
         auto issue_pv = [&](int jj) -> bool {
-            const int st = (kt0 + jj) & 1, use = (kt0 + jj) >> 1;
+            const int st = (kt0 + jj) % VSTAGES, use = (kt0 + jj) / VSTAGES;
             if (!mbar_wait(smem_u32(&b.p_full[pc & 1]), (pc >> 1) & 1, ctx, abort)) return false;
             if (!mbar_wait(smem_u32(&b.v_full[st]), use & 1, ctx, abort)) return false;
             if (jj == 0 && qi >= 1 &&
@@ -301,7 +318,7 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
         };
         for (int j = 0; ok && j < n; ++j) {
             // one S buffer: tile t may start once the softmax has loaded tile t-1
-            const int t = kt0 + j, st = t & 1, use = t >> 1;
+            const int t = kt0 + j, st = t % KSTAGES, use = t / KSTAGES;
             if (t >= 1) ok = mbar_wait(smem_u32(&b.s_empty), (t - 1) & 1, ctx, abort);
             if (ok) ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort);
             if (!ok) break;
@@ -400,6 +417,13 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
         float m_run = null_sink ? sink * LOG2E : -INFINITY;
         float l = null_sink ? 1.0f : 0.0f;
         const uint64_t scale2 = f2_pack(p.scale_l2, p.scale_l2);
+        // warp-level: union of the rows' intervals (for skipping) and their
+        // intersection (chunks inside it need no masking); fixed per item in
+        // window mode, per tile in block mode
+        int wlo = __reduce_min_sync(FULL, lo_r);
+        int whi = __reduce_max_sync(FULL, hi_r);
+        int ilo = __reduce_max_sync(FULL, row_valid ? lo_r : INT_MIN);
+        int ihi = __reduce_min_sync(FULL, row_valid ? hi_r : INT_MAX);
         TileIter<MODE> ti(it);
         for (int j = 0; j < it.ntiles; ++j) {
             const int base = ti.next(p, it);
@@ -412,13 +436,11 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
                     lo_r = NONE_LO;
                     hi_r = NONE_HI;
                 }
+                wlo = __reduce_min_sync(FULL, lo_r);
+                whi = __reduce_max_sync(FULL, hi_r);
+                ilo = __reduce_max_sync(FULL, row_valid ? lo_r : INT_MIN);
+                ihi = __reduce_min_sync(FULL, row_valid ? hi_r : INT_MAX);
             }
-            // warp-level: union of the rows' intervals (for skipping) and
-            // their intersection (chunks inside it need no masking)
-            const int wlo = __reduce_min_sync(FULL, lo_r);
-            const int whi = __reduce_max_sync(FULL, hi_r);
-            const int ilo = __reduce_max_sync(FULL, row_valid ? lo_r : INT_MIN);
-            const int ihi = __reduce_min_sync(FULL, row_valid ? hi_r : INT_MAX);
             if (!mbar_wait(smem_u32(&b.s_full), sc & 1, ctx, abort)) { ok = false; break; }
             tc_fence_after();
             uint32_t x[2][32];
@@ -441,7 +463,7 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
             if (key0 && base == 0 && (live & 1u))
                 x[0][0] = __float_as_uint(__uint_as_float(x[0][0]) + sink * p.inv_scale);
             // mask partial chunks; maximum of the raw scores
-            float mraw = -INFINITY;
+            float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 if (!(live >> c & 1u)) continue;
@@ -453,8 +475,10 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
                 }
 #pragma unroll
                 for (int e = 0; e < 32; e += 2)
-                    mraw = max3(mraw, __uint_as_float(x[c][e]), __uint_as_float(x[c][e + 1]));
+                    mr[(e >> 1) & 3] = max3(mr[(e >> 1) & 3], __uint_as_float(x[c][e]),
+                                            __uint_as_float(x[c][e + 1]));
             }
+            const float mraw = fmaxf(max3(mr[0], mr[1], mr[2]), mr[3]);
             const float mt = mraw * p.scale_l2;
             const bool upd = mt > m_run + TAU;
             float alpha = 1.0f;
@@ -486,7 +510,7 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
             }
             const float mu = (m_run == -INFINITY) ? 0.0f : m_run;
             const uint64_t negm2 = f2_pack(-mu, -mu);
-            uint64_t lsum = f2_pack(0.f, 0.f);
+            uint64_t lsum = f2_pack(0.f, 0.f), lsum2 = f2_pack(0.f, 0.f);
             uint32_t pw[32];  // P as bf16 pairs: word w holds keys 2w (low half) and 2w+1
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
@@ -500,7 +524,8 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
                         f2_unpack(arg, a0, a1);
                         a0 = ex2(a0);
                         a1 = ex2(a1);
-                        lsum = f2_add(lsum, f2_pack(a0, a1));
+                        if (e & 2) lsum2 = f2_add(lsum2, f2_pack(a0, a1));
+                        else lsum = f2_add(lsum, f2_pack(a0, a1));
                         pw[16 * c + e / 2] = pack_bf16x2(a0, a1);
                     }
                 } else {
@@ -509,9 +534,10 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
                 }
             }
             {
-                float s0, s1;
+                float s0, s1, s2, s3;
                 f2_unpack(lsum, s0, s1);
-                l += s0 + s1;
+                f2_unpack(lsum2, s2, s3);
+                l += (s0 + s1) + (s2 + s3);
             }
             tmem_st32(tmem + P_COL + 32u * (uint32_t)(pc & 1) + lane_off, pw);
             tc_wait_st();
@@ -527,33 +553,38 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const size_t orow = (size_t)(it.q_row0 + r) * p.H + it.h;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(o_tmem + 32u * c, ov);
+        for (int half = 0; half < 2; ++half) {
+            uint32_t ov[2][32];
+            tmem_ld32(o_tmem + 64u * half, ov[0]);
+            tmem_ld32(o_tmem + 64u * half + 32u, ov[1]);
             tc_wait_ld();
-            if (c == 3) {  // O fully read: the next item's first P V may overwrite it
+            if (half == 1) {  // O fully read: the next item's first P V may overwrite it
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
             }
             if (!row_valid) continue;
-            if (MODE == MODE_WINDOW) {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * HD + 32 * c);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(ov[8 * u + 0]) * inv, __uint_as_float(ov[8 * u + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(ov[8 * u + 2]) * inv, __uint_as_float(ov[8 * u + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(ov[8 * u + 4]) * inv, __uint_as_float(ov[8 * u + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(ov[8 * u + 6]) * inv, __uint_as_float(ov[8 * u + 7]) * inv);
-                    dst[u] = w;
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * half + cc;
+                if (MODE == MODE_WINDOW) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * HD + 32 * c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 0]) * inv, __uint_as_float(ov[cc][8 * u + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 2]) * inv, __uint_as_float(ov[cc][8 * u + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 4]) * inv, __uint_as_float(ov[cc][8 * u + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 6]) * inv, __uint_as_float(ov[cc][8 * u + 7]) * inv);
+                        dst[u] = w;
+                    }
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + orow * HD + 32 * c);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        dst[u] = make_float4(__uint_as_float(ov[cc][4 * u]) * inv, __uint_as_float(ov[cc][4 * u + 1]) * inv,
+                                             __uint_as_float(ov[cc][4 * u + 2]) * inv, __uint_as_float(ov[cc][4 * u + 3]) * inv);
                 }
-            } else {
-                float4 *dst = reinterpret_cast<float4 *>(p.o_part + orow * HD + 32 * c);
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    dst[u] = make_float4(__uint_as_float(ov[4 * u]) * inv, __uint_as_float(ov[4 * u + 1]) * inv,
-                                         __uint_as_float(ov[4 * u + 2]) * inv, __uint_as_float(ov[4 * u + 3]) * inv);
             }
         }
         if (row_valid) {
@@ -584,9 +615,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSLOTS; ++s) {
             Bars &b = sm.bars[s];
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < KSTAGES; ++i) {
                 mbar_init(smem_u32(&b.k_full[i]), 1);
                 mbar_init(smem_u32(&b.k_empty[i]), 1);
+            }
+            for (int i = 0; i < VSTAGES; ++i) {
                 mbar_init(smem_u32(&b.v_full[i]), 1);
                 mbar_init(smem_u32(&b.v_empty[i]), 1);
             }

@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/sattn.h"
+#include "sattn.h"
 
 namespace sattn {
 
