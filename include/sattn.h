@@ -105,7 +105,9 @@ sattn_status sattn_window_fwd(const void *q, const void *k, const void *v, void 
  *     With a workspace the index list may be split across CTAs and the
  *     partial results merged through their LSE on the device; without one
  *     each query's list is processed by a single CTA.
- * Requirements: d == 128 for BF16 (d in {64, 128} for F32), N >= 1, K >= 0.
+ * Requirements: d == 128 for BF16 (d in {64, 128} for F32), N >= 1, K >= 0;
+ * with BF16, q, kv_cache and o 16-byte aligned (SATTN_ERR_INVALID_ARG
+ * otherwise).
  */
 sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t *topk_idxs,
                               const float *sinks, sattn_sink_mode sink_mode, float scale, void *o,

@@ -234,7 +234,7 @@ sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t
                  (int)dtype};
     cudaStream_t s = as_stream(cuda_stream);
     if (dtype == SATTN_BF16) {
-        if (!aligned16(q) || !aligned16(kv_cache)) return SATTN_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(o)) return SATTN_ERR_INVALID_ARG;
         return finish(launch_sparse_tc(a, *dev, s), s);
     }
     return finish(launch_sparse_simt(a, *dev, s), s);

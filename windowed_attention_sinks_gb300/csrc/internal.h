@@ -79,7 +79,10 @@ struct MergeArgs {
 cudaError_t launch_window_simt(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_sparse_simt(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_block_simt(const BlockArgs &a, const DevInfo &dev, cudaStream_t s);
-cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s);
+// after_primary: launched as a programmatic dependent of the kernel just
+// issued on `s` (that kernel triggers early; the merge waits for its results).
+cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s,
+                         bool after_primary = false);
 
 // tcgen05 kernels: bf16, d = 128.
 cudaError_t launch_window_tc(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);

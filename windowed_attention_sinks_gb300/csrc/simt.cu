@@ -186,6 +186,9 @@ __global__ void __launch_bounds__(kWarps * 32) block_simt_kernel(BlockArgs a, De
 
 template <typename TO>
 __global__ void __launch_bounds__(kWarps * 32) merge_kernel(MergeArgs a) {
+    // When launched as a programmatic dependent, wait until the producing grid
+    // has finished and its writes are visible (returns at once otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (r >= a.R) return;
@@ -261,12 +264,21 @@ cudaError_t launch_block_simt(const BlockArgs &a, const DevInfo &dev, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s) {
+cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s,
+                         bool after_primary) {
     (void)dev;
-    dim3 g = rows_grid(a.R), b(kWarps * 32);
-    if (a.dtype == SATTN_F32) merge_kernel<float><<<g, b, 0, s>>>(a);
-    else merge_kernel<__nv_bfloat16><<<g, b, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = rows_grid(a.R);
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_primary ? 1 : 0;
+    if (a.dtype == SATTN_F32) return cudaLaunchKernelEx(&cfg, merge_kernel<float>, a);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16>, a);
 }
 
 }  // namespace sattn
