@@ -14,17 +14,16 @@
 // are split across CTAs). A persistent grid of one CTA per SM runs two
 // independent slots, each with its own shared memory, TMEM columns,
 // barriers and item stream. Each slot is warp-specialised:
-//   gather warp   reads the list 128 entries ahead and compacts the valid
-//                 ones (0 <= idx < N) into tiles of up to 128 rows, so -1
-//                 entries cost no MMA work; the listed rows are copied with
-//                 16-byte cp.async into a 128B-swizzled K-major tile (rows
-//                 past the tile's count are zero-filled); two stages, each
-//                 completed on an mbarrier.
+//   lead warp     loads Q (TMA) and compacts the valid list entries
+//                 (0 <= idx < N) into tiles of up to 128 rows, so -1 entries
+//                 cost no MMA work; tiles go through a 3-entry ring.
+//   copy warps    copy each tile's rows with 16-byte cp.async into a
+//                 128B-swizzled K-major stage (rows past the count are
+//                 zero-filled); two stages, completed on an mbarrier.
 //   MMA thread    S^T of tile t into one of two S buffers, then
 //                 O^T += KV^T P^T for tile t-1, so the tensor core works on
 //                 the next scores while the softmax runs.
-//   4 warps       softmax: S^T is transposed through shared memory so that
-//                 four threads own one head (two shuffles per reduction);
+//   4 warps       softmax, one head per lane after a per-warp transpose;
 //                 running max / sum per head in the log2 domain, P (bf16)
 //                 to a double-buffered shared tile; epilogue O^T / l.
 // Summation order differs from list order (compaction); softmax does not
@@ -44,17 +43,25 @@ constexpr int R = 128;         // gathered rows per tile
 constexpr int HD = 128;        // head dim
 constexpr int NH = 32;         // query heads handled by the kernel
 constexpr int NSLOT = 2;         // independent item streams per CTA
-constexpr int GATHER_WARPS = 4;  // per slot; one warp issues cp.async at ~10 B/clk at most
-constexpr int SLOT_CTRL = GATHER_WARPS + 1;  // gather warps + the MMA warp of a slot
+// Per slot: one warp compacts index lists, GATHER_WARPS warps copy rows (one
+// warp issues cp.async at ~10 B/clk at most, and index loads queued behind a
+// warp's copies would stall its compaction), one warp issues the MMAs.
+constexpr int GATHER_WARPS = 4;
+constexpr int SLOT_CTRL = GATHER_WARPS + 2;  // control warps of a slot
+// Compacted-index ring depth. The lead gather warp compacts tile t+1 only
+// after acquiring the KV stage of tile t, i.e. after P V of tile t-2 is
+// complete, and every reader of ring entry (t+1) % 3 (copies, MMA, softmax of
+// tile t-2) is done by then.
+constexpr int IDX_RING = 3;
 constexpr int NTHREADS = 32 * NSLOT * (SLOT_CTRL + 4);
 constexpr int SOFTMAX_THREADS = 128;
 constexpr uint32_t KV_TILE = R * HD * 2;   // 32 KB
 constexpr uint32_t KV_HALF = KV_TILE / 2;  // 64 columns of d
 constexpr uint32_t QP_HALF = NH * 128;     // 4 KB: one 64-column half of Q or P
-// Transpose buffer: head h, row quarter q, entry i at h * SB_HEAD + q * SB_PART + i.
-// Row writes (fixed h) are consecutive; the 16-byte reads of the 8 threads
-// sharing an LDS.128 phase fall in distinct bank groups (39h + 10q mod 8).
-constexpr int SB_HEAD = 156, SB_PART = 40;
+// Per-warp transpose buffer: head h, key i of the warp at h * TB_STRIDE + i.
+// Writes (one head, 32 keys) are consecutive; the 16-byte reads of the 8
+// lanes sharing an LDS.128 phase fall in distinct bank groups (9h + k mod 8).
+constexpr int TB_STRIDE = 36;
 constexpr float TAU = 8.0f;
 constexpr int MAX_SPLITS = 64;
 constexpr uint32_t SLOT_COLS = 128;  // TMEM per slot: S^T[2] (32 each), O^T (32)
@@ -62,6 +69,7 @@ constexpr uint32_t TMEM_COLS = SLOT_COLS * NSLOT;
 constexpr uint32_t S_COL = 0, O_COL = 64;
 
 struct SlotBars {
+    uint64_t idx_ready[IDX_RING];  // lead gather warp -> the other gather warps
     uint64_t q_full, q_empty;
     uint64_t kv_full[2], kv_empty[2];
     uint64_t s_full[2], s_empty[2];
@@ -74,15 +82,16 @@ struct alignas(1024) SlotSmem {
     uint8_t kv[2][KV_TILE];
     uint8_t q[2 * QP_HALF];
     uint8_t p[2][2 * QP_HALF];
-    float sbuf[NH * SB_HEAD];
-    // compacted entries of the tile in each stage (-1 past the count), one
-    // copy per gather warp; the softmax reads copy 0
-    int idx[GATHER_WARPS][2][R];
-    int tile_cnt[2];    // rows that hold entries
-    int tile_last[2];   // the tile in this stage ends its item
+    float tbuf[4][NH * TB_STRIDE];
+    // Ring of compacted tiles: tile t uses entry t % IDX_RING
+    int idx[IDX_RING][R];    // entries (-1 past the count)
+    int tile_cnt[IDX_RING];  // rows that hold entries
+    int tile_last[IDX_RING]; // the tile ends its item
+    int tile_row0[IDX_RING]; // first cache row of the tile's request; -1: no more tiles
+    float xmax[4][NH];   // per-warp tile maxima (max update only)
+    float lpart[4][NH];  // per-warp partial denominators (epilogue)
     float alpha[NH];
-    float m[NH];
-    float l[NH];
+    float inv_l[NH];
     SlotBars b;
 };
 
@@ -169,38 +178,77 @@ __device__ __forceinline__ ItemInfo item_info(const SpParams &p, int item) {
 
 // ------------------------------------------------------------------ gather warp
 
-// Every gather warp of a slot compacts the same index lists (the result is
-// deterministic, so no warp waits for another); warp g copies rows
-// 64g .. 64g+63 of each tile. Warp 0 also loads Q and publishes the tile's
-// indices, count and last flag for the MMA and softmax roles.
-__device__ void gather_role(const SpParams &p, const CUtensorMap *tq, SlotSmem &sm,
-                            volatile int *abort, int g, int first, int stride,
-                            const DevCtx &ctx) {
+// Copy warp g of a slot copies rows 2i + hi, i in [PAIRS g, PAIRS (g+1)), of
+// each tile. The lead warp loads Q, compacts the index lists into the ring
+// and publishes each ring entry to the copy warps (idx_ready) and, once the
+// tile's stage is free, to the MMA and softmax roles (kv_full); after the
+// last tile it publishes an entry with tile_row0 = -1.
+constexpr int PAIRS = R / 2 / GATHER_WARPS;  // row pairs per warp (multiple of 4)
+
+struct RowCopier {
+    uint32_t dofs[4];
+    int hi, unit;
+    // lane = (hi, unit) copies 16-byte unit `unit` of rows 2i + hi. In the 128B
+    // swizzle, unit u of row r sits at r * 128 + ((u ^ (r & 7)) << 4), and
+    // (unit & 7) ^ (r & 7) = ((unit & 7) ^ hi) ^ (2i & 6): four lane offsets
+    // cover every i.
+    __device__ explicit RowCopier(int lane) {
+        hi = lane >> 4;
+        unit = lane & 15;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            dofs[c] = (uint32_t)(unit >> 3) * KV_HALF + (uint32_t)hi * 128u +
+                      ((((uint32_t)(unit & 7) ^ (uint32_t)hi) ^ (uint32_t)(2 * c)) << 4);
+    }
+    // this warp's rows of one tile; entries of -1 are zero-filled so that P V
+    // stays finite
+    __device__ void issue(uint32_t kv_s, const int *ids, const __nv_bfloat16 *rows, int g) const {
+        const __nv_bfloat16 *src0 = rows + unit * 8;
+#pragma unroll
+        for (int i2 = 0; i2 < PAIRS; ++i2) {
+            const int i = PAIRS * g + i2;
+            const int e = ids[2 * i + hi];
+            cp_async16(kv_s + dofs[i2 & 3] + (uint32_t)i * 256u,
+                       src0 + (size_t)(e >= 0 ? e : 0) * HD, e >= 0 ? 16u : 0u);
+        }
+    }
+};
+
+// warp-uniform bounded wait (lane 0 polls)
+__device__ __forceinline__ bool warp_wait(uint64_t &bar, int parity, const DevCtx &ctx,
+                                          volatile int *abort) {
+    int r = 1;
+    if ((threadIdx.x & 31) == 0) r = mbar_wait(smem_u32(&bar), (uint32_t)parity, ctx, abort) ? 1 : 0;
+    r = __shfl_sync(0xffffffffu, r, 0);
+    __syncwarp();
+    return r != 0;
+}
+
+__device__ void gather_helper(const SpParams &p, SlotSmem &sm, volatile int *abort, int g,
+                              const DevCtx &ctx) {
     SlotBars &b = sm.b;
-    const bool lead = g == 0;
+    const RowCopier cp(threadIdx.x & 31);
+    for (int t = 0;; ++t) {
+        const int r = t % IDX_RING, st = t & 1, use = t >> 1;
+        if (!warp_wait(b.idx_ready[r], (t / IDX_RING) & 1, ctx, abort)) break;
+        const int row0 = sm.tile_row0[r];
+        if (row0 < 0) break;
+        if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) break;
+        cp.issue(smem_u32(sm.kv[st]), sm.idx[r], p.kv + (size_t)row0 * HD, g);
+        cp_async_arrive(smem_u32(&b.kv_full[st]));
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+}
+
+__device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &sm,
+                            volatile int *abort, int first, int stride, const DevCtx &ctx) {
+    SlotBars &b = sm.b;
     const int lane = threadIdx.x & 31;
     const uint32_t lt_mask = (1u << lane) - 1u;
     const int nitems = p.B * p.M * p.splits;
     int qi = 0, gt = 0;  // items started, tiles issued
     bool ok = true, bad = false;
-    // Row copies: lane = (hi, unit) copies 16-byte unit `unit` of rows 2i + hi.
-    // In the 128B swizzle, unit u of row r sits at r * 128 + ((u ^ (r & 7)) << 4),
-    // and (unit & 7) ^ (r & 7) = ((unit & 7) ^ hi) ^ (2i & 6): four lane offsets
-    // cover every i.
-    const int hi = lane >> 4, unit = lane & 15;
-    uint32_t dofs[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        dofs[c] = (uint32_t)(unit >> 3) * KV_HALF + (uint32_t)hi * 128u +
-                  ((((uint32_t)(unit & 7) ^ (uint32_t)hi) ^ (uint32_t)(2 * c)) << 4);
-    // warp-uniform bounded wait (lane 0 polls)
-    auto wwait = [&](uint64_t &bar, int parity) -> bool {
-        int r = 1;
-        if (lane == 0) r = mbar_wait(smem_u32(&bar), (uint32_t)parity, ctx, abort) ? 1 : 0;
-        r = __shfl_sync(0xffffffffu, r, 0);
-        __syncwarp();
-        return r != 0;
-    };
     // pull an item's slice of the index list into L2 ahead of its use
     auto prefetch_list = [&](int item) {
         if (item >= nitems) return;
@@ -210,111 +258,106 @@ __device__ void gather_role(const SpParams &p, const CUtensorMap *tq, SlotSmem &
         for (int off = lane * 128; off < bytes; off += 32 * 128)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
     };
-    if (lead) {
-        if (lane == 0) prefetch_tmap(tq);
-        prefetch_list(first);
-    }
+    if (lane == 0) prefetch_tmap(tq);
+    prefetch_list(first);
     for (int item = first; ok && item < nitems; item += stride) {
         const ItemInfo it = item_info(p, item);
         const int32_t *list = p.idx + (size_t)it.bm * p.K;
-        const __nv_bfloat16 *kvb = p.kv + (size_t)it.b * p.N * HD + unit * 8;
-        if (lead) {
-            prefetch_list(item + stride);
-            // Q rows of the query (32 heads x 256 B): two 64-column boxes
-            if (qi >= 1 && !wwait(b.q_empty, (qi - 1) & 1)) { ok = false; break; }
-            if (lane == 0) {
-                const uint32_t bar = smem_u32(&b.q_full);
-                mbar_arrive_expect_tx(bar, 2 * QP_HALF);
-                tma_load_2d(smem_u32(sm.q), tq, bar, 0, it.bm * NH);
-                tma_load_2d(smem_u32(sm.q) + QP_HALF, tq, bar, 64, it.bm * NH);
-            }
-            ++qi;
+        const int row0 = it.b * p.N;  // first cache row of this request
+        prefetch_list(item + stride);
+        // Q rows of the query (32 heads x 256 B): two 64-column boxes
+        if (qi >= 1 && !warp_wait(b.q_empty, (qi - 1) & 1, ctx, abort)) { ok = false; break; }
+        if (lane == 0) {
+            const uint32_t bar = smem_u32(&b.q_full);
+            mbar_arrive_expect_tx(bar, 2 * QP_HALF);
+            tma_load_2d(smem_u32(sm.q), tq, bar, 0, it.bm * NH);
+            tma_load_2d(smem_u32(sm.q) + QP_HALF, tq, bar, 64, it.bm * NH);
         }
-        auto acquire = [&]() -> bool {  // the stage of tile gt is free
-            const int use = gt >> 1;
-            return use == 0 || wwait(b.kv_empty[gt & 1], (use - 1) & 1);
-        };
-        // Issue the tile in stage gt & 1 holding `pos` compacted rows; rows past
-        // the count are zero-filled so that P V stays finite.
-        auto close_tile = [&](int pos, bool last) {
-            const int st = gt & 1;
-            int *ids = sm.idx[g][st];
+        ++qi;
+        int ring = gt % IDX_RING;  // ring entry of the tile being compacted
+        // Publish and issue the compacted tile gt holding `pos` rows.
+        auto close_tile = [&](int pos, bool last) -> bool {
+            const int st = gt & 1, use = gt >> 1;
+            int *ids = sm.idx[ring];
             for (int r = pos + lane; r < R; r += 32) ids[r] = -1;
-            if (lead && lane == 0) {
-                sm.tile_cnt[st] = pos;
-                sm.tile_last[st] = last ? 1 : 0;
+            if (lane == 0) {
+                sm.tile_cnt[ring] = pos;
+                sm.tile_last[ring] = last ? 1 : 0;
+                sm.tile_row0[ring] = row0;
             }
             __syncwarp();
-            const uint32_t kv_s = smem_u32(sm.kv[st]);
-            constexpr int PAIRS = R / 2 / GATHER_WARPS;  // row pairs per warp (multiple of 4)
-#pragma unroll 16
-            for (int i2 = 0; i2 < PAIRS; ++i2) {
-                const int i = PAIRS * g + i2;
-                const int e = ids[2 * i + hi];
-                cp_async16(kv_s + dofs[i2 & 3] + (uint32_t)i * 256u,
-                           kvb + (size_t)(e >= 0 ? e : 0) * HD, e >= 0 ? 16u : 0u);
-            }
-            const uint32_t bar = smem_u32(&b.kv_full[st]);
-            cp_async_arrive(bar);
-            __syncwarp();
-            if (lead && lane == 0) mbar_arrive(bar);  // publishes idx, tile_cnt, tile_last
+            if (lane == 0) mbar_arrive(smem_u32(&b.idx_ready[ring]));
+            // kv_full of this stage may take this arrival only once the stage's
+            // previous tile is consumed (which also keeps the ring safe)
+            if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) return false;
+            if (lane == 0) mbar_arrive(smem_u32(&b.kv_full[st]));  // ring entry -> MMA, softmax
             ++gt;
+            ring = gt % IDX_RING;
+            return true;
         };
+        // Index loads are only issued here (addresses clamped into the slice);
+        // their values are first used, and validated, one group later.
         auto load = [&](int (&v)[4], int e0) {
 #pragma unroll
+            for (int c = 0; c < 4; ++c) v[c] = __ldg(list + min(e0 + 32 * c + lane, it.e_end - 1));
+        };
+        int pos = 0;
+        // compact one group of 128 entries (starting at e0) into the open tile
+        auto compact = [&](const int (&v)[4], int e0) {
+#pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int e = e0 + 32 * c + lane;
-                int x = e < it.e_end ? __ldg(list + e) : -1;
-                if (x < -1 || x >= p.N) {
+                int x = v[c];
+                if (e0 + 32 * c + lane >= it.e_end) {
+                    x = -1;
+                } else if (x < -1 || x >= p.N) {
                     bad = true;
                     x = -1;
                 }
-                v[c] = x;
-            }
-        };
-        int pos = 0;
-        // compact one group of 128 entries into the open tile
-        auto compact = [&](const int (&v)[4]) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const bool valid = v[c] >= 0;
+                const bool valid = x >= 0;
                 const uint32_t bal = __ballot_sync(0xffffffffu, valid);
                 const int cnt = __popc(bal);
                 if (cnt == 0) continue;
                 if (pos + cnt > R) {  // does not fit: issue this tile, open the next
                     __syncwarp();
-                    close_tile(pos, false);
-                    if (!acquire()) {
+                    if (!close_tile(pos, false)) {
                         ok = false;
                         return;
                     }
                     pos = 0;
                 }
-                if (valid) sm.idx[g][gt & 1][pos + __popc(bal & lt_mask)] = v[c];
+                if (valid) sm.idx[ring][pos + __popc(bal & lt_mask)] = x;
                 pos += cnt;
             }
         };
-        if (!acquire()) { ok = false; break; }
-        // two groups of indices in flight: each is loaded one group ahead of use
-        int va[4], vb[4];
-        load(va, it.e_begin);
-        load(vb, it.e_begin + R);
-        for (int e0 = it.e_begin; ok && e0 < it.e_end; e0 += 2 * R) {
-            compact(va);
-            load(va, e0 + 2 * R);
-            if (!ok || e0 + R >= it.e_end) break;
-            compact(vb);
-            load(vb, e0 + 3 * R);
+        if (it.e_end > it.e_begin) {
+            // two groups of indices in flight: each is loaded one group ahead of use
+            int va[4], vb[4];
+            load(va, it.e_begin);
+            load(vb, it.e_begin + R);
+            for (int e0 = it.e_begin; ok && e0 < it.e_end; e0 += 2 * R) {
+                compact(va, e0);
+                load(va, e0 + 2 * R);
+                if (!ok || e0 + R >= it.e_end) break;
+                compact(vb, e0 + R);
+                load(vb, e0 + 3 * R);
+            }
         }
         if (!ok) break;
         __syncwarp();
-        close_tile(pos, true);  // an item without valid entries still gets one (empty) tile
+        // an item without valid entries still gets one (empty) tile
+        if (!close_tile(pos, true)) { ok = false; break; }
     }
-    if (bad && lead) record_error(ctx, DEVERR_INDEX);
-    // copies in flight land before the CTA may exit (on the normal path all of
-    // them were consumed already; this matters after an abort)
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    if (lead && lane == 0 && qi >= 1) {
+    if (ok) {  // no more tiles (the ring entry is free: see IDX_RING)
+        const int ring = gt % IDX_RING;
+        if (lane == 0) {
+            sm.tile_row0[ring] = -1;
+            mbar_arrive(smem_u32(&b.idx_ready[ring]));
+        }
+    }
+    if (bad) record_error(ctx, DEVERR_INDEX);
+    // the last Q load lands before the CTA may exit (on the normal path it was
+    // consumed already; this matters after an abort)
+    if (lane == 0 && qi >= 1) {
         int zero = 0;
         mbar_wait(smem_u32(&b.q_full), (qi - 1) & 1, ctx, &zero);
     }
@@ -323,57 +366,88 @@ __device__ void gather_role(const SpParams &p, const CUtensorMap *tq, SlotSmem &
 
 // ------------------------------------------------------------------ MMA thread
 
+// The MMA thread issues in readiness order: S^T of the next tile as soon as
+// its rows have landed (and its S buffer and Q are free), O^T += KV^T P^T of
+// the oldest pending tile as soon as its P is written. Issuing S before P V in
+// program order instead would hold P V of tile t behind the gather of tile
+// t+1, which itself waits for P V of tile t-1 to free its stage.
+// S(t) needs kv_full(t), hence P V of tile t-2 complete: the S cursor runs at
+// most two tiles ahead of the P V cursor.
 __device__ void mma_role(const SpParams &p, SlotSmem &sm, volatile int *abort, uint32_t tmem,
                          int first, int stride, const DevCtx &ctx) {
     SlotBars &b = sm.b;
     const int nitems = p.B * p.M * p.splits;
+    const int my_items = first < nitems ? (nitems - first + stride - 1) / stride : 0;
     const uint32_t q_base = smem_u32(sm.q), t_o = tmem + O_COL;
-    int qi = 0, gt = 0;
-    bool ok = true;
-    for (int item = first; ok && item < nitems; item += stride) {
-        if (!mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort)) break;
-        const int gt0 = gt;
-        // O^T += KV^T P^T for tile jj of this item
-        auto issue_pv = [&](int jj) -> bool {
-            const int t = gt0 + jj, st = t & 1;
-            if (!mbar_wait(smem_u32(&b.p_full[st]), (t >> 1) & 1, ctx, abort)) return false;
-            if (jj == 0 && qi >= 1 &&
-                !mbar_wait(smem_u32(&b.o_empty), (qi - 1) & 1, ctx, abort))
-                return false;
-            tc_fence_after();
-            const uint32_t kv_s = smem_u32(sm.kv[st]), p_s = smem_u32(sm.p[st]);
+    int s_t = 0, s_item = 0;     // next tile / item for S
+    int pv_t = 0, pv_item = 0;   // next tile / item for P V
+    bool s_first = true, pv_first = true;  // the next tile opens its item
+    uint32_t lastmask = 0;       // bit t & 3: tile t closes its item (known once S(t) issued)
+    uint64_t stall_t0 = 0;
+    uint32_t spins = 0;
+    while (pv_item < my_items) {
+        bool progress = false;
+        if (s_item < my_items) {
+            const int st = s_t & 1, use = s_t >> 1;
+            if ((!s_first || mbar_try_wait(smem_u32(&b.q_full), s_item & 1)) &&
+                (use == 0 || mbar_try_wait(smem_u32(&b.s_empty[st]), (use - 1) & 1)) &&
+                mbar_try_wait(smem_u32(&b.kv_full[st]), use & 1)) {
+                tc_fence_after();
+                const bool last = sm.tile_last[s_t % IDX_RING] != 0;
+                const uint32_t kv_s = smem_u32(sm.kv[st]);
 #pragma unroll
-            for (int kk = 0; kk < R / 16; ++kk)
-                tc_mma_f16(t_o, desc_mn(kv_s, kk), desc_k(p_s, kk, QP_HALF), IDESC_O,
-                           (jj > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(smem_u32(&b.kv_empty[st]));
-            tc_commit(smem_u32(&b.p_empty[st]));
-            tc_commit(smem_u32(&b.pv_done));
-            return true;
-        };
-        int j = 0;
-        for (bool last = false; !last; ++j) {
-            const int t = gt0 + j, st = t & 1, use = t >> 1;
-            if (use >= 1 && !mbar_wait(smem_u32(&b.s_empty[st]), (use - 1) & 1, ctx, abort)) {
-                ok = false;
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    tc_mma_f16(tmem + S_COL + 32u * st, desc_k(kv_s, kk, KV_HALF),
+                               desc_k(q_base, kk, QP_HALF), IDESC_S, kk > 0 ? 1u : 0u);
+                tc_commit(smem_u32(&b.s_full[st]));
+                if (last) {
+                    tc_commit(smem_u32(&b.q_empty));
+                    lastmask |= 1u << (s_t & 3);
+                    ++s_item;
+                } else {
+                    lastmask &= ~(1u << (s_t & 3));
+                }
+                s_first = last;
+                ++s_t;
+                progress = true;
+            }
+        }
+        if (pv_t < s_t) {
+            const int st = pv_t & 1;
+            if (mbar_try_wait(smem_u32(&b.p_full[st]), (pv_t >> 1) & 1) &&
+                (!pv_first || pv_item == 0 ||
+                 mbar_try_wait(smem_u32(&b.o_empty), (pv_item - 1) & 1))) {
+                tc_fence_after();
+                const uint32_t kv_s = smem_u32(sm.kv[st]), p_s = smem_u32(sm.p[st]);
+#pragma unroll
+                for (int kk = 0; kk < R / 16; ++kk)
+                    tc_mma_f16(t_o, desc_mn(kv_s, kk), desc_k(p_s, kk, QP_HALF), IDESC_O,
+                               (!pv_first || kk > 0) ? 1u : 0u);
+                tc_commit(smem_u32(&b.kv_empty[st]));
+                tc_commit(smem_u32(&b.p_empty[st]));
+                tc_commit(smem_u32(&b.pv_done));
+                const bool last = (lastmask >> (pv_t & 3)) & 1u;
+                if (last) {
+                    tc_commit(smem_u32(&b.o_full));
+                    ++pv_item;
+                }
+                pv_first = last;
+                ++pv_t;
+                progress = true;
+            }
+        }
+        if (progress) {
+            spins = 0;
+        } else if ((++spins & 63u) == 0) {  // bounded: give up after the wait limit
+            if (*abort) break;
+            const uint64_t now = global_timer_ns();
+            if (spins == 64) stall_t0 = now;
+            else if (now - stall_t0 > ctx.wait_ns) {
+                *abort = 1;
+                record_error(ctx, DEVERR_TIMEOUT);
                 break;
             }
-            if (!mbar_wait(smem_u32(&b.kv_full[st]), use & 1, ctx, abort)) { ok = false; break; }
-            tc_fence_after();
-            last = sm.tile_last[st] != 0;
-            const uint32_t kv_s = smem_u32(sm.kv[st]);
-#pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk)
-                tc_mma_f16(tmem + S_COL + 32u * st, desc_k(kv_s, kk, KV_HALF),
-                           desc_k(q_base, kk, QP_HALF), IDESC_S, kk > 0 ? 1u : 0u);
-            tc_commit(smem_u32(&b.s_full[st]));
-            if (last) tc_commit(smem_u32(&b.q_empty));
-            if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
         }
-        if (!ok || !issue_pv(j - 1)) break;
-        tc_commit(smem_u32(&b.o_full));
-        gt = gt0 + j;
-        ++qi;
     }
     // every MMA issued so far completes before TMEM is released
     tc_commit(smem_u32(&b.drain));
@@ -383,23 +457,30 @@ __device__ void mma_role(const SpParams &p, SlotSmem &sm, volatile int *abort, u
 
 // ------------------------------------------------------------------ softmax warps
 
+// Softmax of one slot: warp w reads S^T rows (keys) 32w .. 32w+31 from TMEM and
+// transposes its own 32 x 32 block through shared memory, so that lane l owns
+// head l over those 32 keys. All warps share one running max per head, which
+// moves only when some warp's tile max exceeds it by more than TAU (log2
+// units): the common case needs a single barrier per tile (an OR over that
+// condition); the max exchange, the O^T rescale and their barriers run only
+// when it is true. Each warp keeps its own partial denominator per head; the
+// four are added in the epilogue.
 __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abort, int slot,
                              uint32_t tmem, int first, int stride, const DevCtx &ctx) {
     SlotBars &b = sm.b;
-    // tid: position in the slot's softmax group (head ownership, stores);
-    // a warp may only access TMEM lanes 32 * (warp id mod 4) .. +31, so this
-    // thread's S^T row / O^T row (head-dim index) is 32 * quarter + lane
-    const int tid = threadIdx.x - 32 * NSLOT * SLOT_CTRL - SOFTMAX_THREADS * slot;
+    // a warp may only access TMEM lanes 32 * (warp id mod 4) .. +31: this
+    // warp's S^T rows (keys) and O^T rows (head-dim indices) are 32 * quarter + lane
     const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
+    const int h = lane;  // head owned after the transpose
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_o = tmem + O_COL + lane_off;
-    const int h = tid >> 2, part = tid & 3;  // head owned (with 3 siblings) and its row quarter
     const bool key0 = p.sink_mode == 1;
     const float sink_h = p.sinks ? __ldg(p.sinks + h) * LOG2E : 0.0f;
     const float bias_raw = key0 ? sink_h / p.scale_l2 : 0.0f;
     const uint64_t scale2 = f2_pack(p.scale_l2, p.scale_l2);
     const bool null_sink = p.sink_mode == 2 && p.splits == 1;
     const int nitems = p.B * p.M * p.splits;
+    float *tb = sm.tbuf[quarter];
     int qi = 0, gt = 0;
     // A failed wait is carried to the next barrier, whose OR makes the exit
     // uniform over the four warps (no thread is left behind at a barrier).
@@ -407,13 +488,14 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
     for (int item = first; item < nitems; item += stride) {
         const ItemInfo it = item_info(p, item);
         float m_run = null_sink ? sink_h : -INFINITY;
-        float l_run = null_sink ? 1.0f : 0.0f;
+        // the null logit's exp(sink - m) = 1 is counted once, in warp 0's partial
+        float l_run = (null_sink && quarter == 0) ? 1.0f : 0.0f;
         const int gt0 = gt;
         int j = 0;
         for (bool last = false; !last; ++j) {
-            const int t = gt0 + j, st = t & 1, use = t >> 1;
-            // S^T of this tile -> transpose buffer; the tile's indices were
-            // published with its gather; P buffer st was last read by P V of tile t-2
+            const int t = gt0 + j, st = t & 1, use = t >> 1, ring = t % IDX_RING;
+            // S^T of this tile; its ring entry was published with kv_full; P
+            // buffer st was last read by P V of tile t-2
             if (!failed) {
                 failed = !mbar_wait(smem_u32(&b.s_full[st]), use & 1, ctx, abort) ||
                          !mbar_wait(smem_u32(&b.kv_full[st]), use & 1, ctx, abort) ||
@@ -421,6 +503,8 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
                           !mbar_wait(smem_u32(&b.p_empty[st]), (use - 1) & 1, ctx, abort));
             }
             failed = __any_sync(0xffffffffu, failed);  // tcgen05.ld is warp-collective
+            float x[32];
+            float mt = -INFINITY;
             if (!failed) {
                 tc_fence_after();
                 uint32_t sv[32];
@@ -429,61 +513,83 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&b.s_empty[st]));
+                // row (key 32 quarter + lane) -> column lane of the warp's block
 #pragma unroll
-                for (int hh = 0; hh < NH; ++hh)
-                    sm.sbuf[hh * SB_HEAD + quarter * SB_PART + lane] = __uint_as_float(sv[hh]);
-            }
-            if (softmax_sync_or(slot, failed)) { failed = true; break; }
-            last = sm.tile_last[st] != 0;
-            // head h over rows part*32 .. part*32+31 (raw scores; scale > 0, so
-            // the max is taken before scaling)
-            float x[32];
-            {
-                const float *src = &sm.sbuf[h * SB_HEAD + part * SB_PART];
+                for (int hh = 0; hh < NH; ++hh) tb[hh * TB_STRIDE + lane] = __uint_as_float(sv[hh]);
+                __syncwarp();
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    const float4 f = *reinterpret_cast<const float4 *>(src + 4 * k);
+                    const float4 f = *reinterpret_cast<const float4 *>(tb + h * TB_STRIDE + 4 * k);
                     x[4 * k] = f.x;
                     x[4 * k + 1] = f.y;
                     x[4 * k + 2] = f.z;
                     x[4 * k + 3] = f.w;
                 }
-            }
-            if (key0) {  // the sink bias on the logit of key 0, in raw-score units
-                const int *ids = &sm.idx[0][st][part * 32];
+                last = sm.tile_last[ring] != 0;
+                if (key0) {  // the sink bias on the logit of key 0, in raw-score units
+                    const int *ids = &sm.idx[ring][quarter * 32];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int4 e = *reinterpret_cast<const int4 *>(ids + 4 * k);
-                    x[4 * k] += e.x == 0 ? bias_raw : 0.f;
-                    x[4 * k + 1] += e.y == 0 ? bias_raw : 0.f;
-                    x[4 * k + 2] += e.z == 0 ? bias_raw : 0.f;
-                    x[4 * k + 3] += e.w == 0 ? bias_raw : 0.f;
+                    for (int k = 0; k < 8; ++k) {
+                        const int4 e = *reinterpret_cast<const int4 *>(ids + 4 * k);
+                        x[4 * k] += e.x == 0 ? bias_raw : 0.f;
+                        x[4 * k + 1] += e.y == 0 ? bias_raw : 0.f;
+                        x[4 * k + 2] += e.z == 0 ? bias_raw : 0.f;
+                        x[4 * k + 3] += e.w == 0 ? bias_raw : 0.f;
+                    }
                 }
-            }
-            const int nvalid = sm.tile_cnt[st] - part * 32;  // rows of this quarter holding entries
-            if (nvalid < 32) {
+                const int nvalid = sm.tile_cnt[ring] - quarter * 32;  // keys of this warp holding entries
+                if (nvalid < 32) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i >= nvalid) x[i] = -INFINITY;
-            }
-            float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    for (int i = 0; i < 32; ++i)
+                        if (i >= nvalid) x[i] = -INFINITY;
+                }
+                // raw scores: scale > 0, so the max is taken before scaling
+                float mr[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) mr[(i >> 1) & 3] = max3(mr[(i >> 1) & 3], x[i], x[i + 1]);
-            float mt = fmaxf(max3(mr[0], mr[1], mr[2]), mr[3]);
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-            mt *= p.scale_l2;
-            const bool upd = mt > m_run + TAU;
-            float alpha = 1.0f;
-            if (upd) {
-                alpha = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mt);
-                l_run *= alpha;
-                m_run = mt;
+                for (int i = 0; i < 32; i += 2)
+                    mr[(i >> 1) & 3] = max3(mr[(i >> 1) & 3], x[i], x[i + 1]);
+                mt = fmaxf(max3(mr[0], mr[1], mr[2]), mr[3]) * p.scale_l2;
+            }
+            // one barrier per tile: does any head of any warp need a new max?
+            // (also orders this tile's transpose reads before the next writes)
+            if (softmax_sync_or(slot, failed || mt > m_run + TAU)) {
+                if (softmax_sync_or(slot, failed)) { failed = true; break; }
+                sm.xmax[quarter][h] = mt;
+                softmax_sync_or(slot, 0);
+                const float mall = fmaxf(fmaxf(sm.xmax[0][h], sm.xmax[1][h]),
+                                         fmaxf(sm.xmax[2][h], sm.xmax[3][h]));
+                const bool upd = mall > m_run + TAU;  // the same in every warp
+                float alpha = 1.0f;
+                if (upd) {
+                    alpha = (m_run == -INFINITY) ? 0.0f : ex2(m_run - mall);
+                    l_run *= alpha;
+                    m_run = mall;
+                }
+                if (quarter == 0) sm.alpha[h] = alpha;
+                if (softmax_sync_or(slot, upd && j >= 1)) {
+                    // rescale the O^T columns (heads) whose max moved, once P V of
+                    // the previous tile is complete (the one before it is: P
+                    // buffer st was free)
+                    failed = __any_sync(0xffffffffu,
+                                        !mbar_wait(smem_u32(&b.pv_done), (t - 1) & 1, ctx, abort));
+                    if (!failed) {
+                        tc_fence_after();
+                        uint32_t ov[32];
+                        tmem_ld32(t_o, ov);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int hh = 0; hh < NH; ++hh)
+                            ov[hh] = __float_as_uint(__uint_as_float(ov[hh]) * sm.alpha[hh]);
+                        tmem_st32(t_o, ov);
+                        tc_wait_st();
+                    }
+                }
             }
             const float mu = m_run == -INFINITY ? 0.0f : m_run;
             const uint64_t negm2 = f2_pack(-mu, -mu);
             uint64_t ls2a = f2_pack(0.f, 0.f), ls2b = ls2a;
-            const uint32_t pbase = smem_u32(sm.p[st]) + (uint32_t)(part >> 1) * QP_HALF;
+            // P^T: head h, keys 32 quarter .. +31 = 64 bytes of one K-major row
+            const uint32_t pbase = smem_u32(sm.p[st]) + (uint32_t)(quarter >> 1) * QP_HALF;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 uint32_t w[4];
@@ -498,39 +604,15 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
                     else ls2a = f2_add(ls2a, f2_pack(a0, a1));
                     w[e2] = pack_bf16x2(a0, a1);
                 }
-                const uint32_t addr = pbase + sw128_offset(h, (part & 1) * 4 + u);
+                const uint32_t addr = pbase + sw128_offset(h, (quarter & 1) * 4 + u);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]),
                              "r"(w[1]), "r"(w[2]), "r"(w[3])
                              : "memory");
             }
-            float ls;
             {
                 float a0, a1;
                 f2_unpack(f2_add(ls2a, ls2b), a0, a1);
-                ls = a0 + a1;
-            }
-            ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-            ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-            l_run += ls;
-            if (part == 0) sm.alpha[h] = alpha;
-            // also orders this tile's transpose-buffer reads before the next tile's writes
-            const int any_upd = softmax_sync_or(slot, upd && j >= 1);
-            if (any_upd) {  // rescale O^T columns (heads) whose max moved
-                // P V of the previous tile must be complete (the one before it
-                // is: P buffer st was free)
-                failed = __any_sync(0xffffffffu,
-                                    !mbar_wait(smem_u32(&b.pv_done), (t - 1) & 1, ctx, abort));
-                if (!failed) {
-                    tc_fence_after();
-                    uint32_t ov[32];
-                    tmem_ld32(t_o, ov);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int hh = 0; hh < NH; ++hh)
-                        ov[hh] = __float_as_uint(__uint_as_float(ov[hh]) * sm.alpha[hh]);
-                    tmem_st32(t_o, ov);
-                    tc_wait_st();
-                }
+                l_run += a0 + a1;
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -542,12 +624,20 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
         // wait comes before the barrier so that a failure leaves uniformly
         if (!failed)
             failed = __any_sync(0xffffffffu, !mbar_wait(smem_u32(&b.o_full), qi & 1, ctx, abort));
-        if (part == 0) {  // per head: 1 / l and the lse (natural log)
-            sm.l[h] = l_run > 0.f ? 1.0f / l_run : 0.f;
-            sm.m[h] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
-        }
+        sm.lpart[quarter][h] = l_run;
         if (softmax_sync_or(slot, failed)) break;
         ++qi;
+        const size_t rows = (size_t)p.B * p.M * NH;
+        if (quarter == 0) {  // head h: total denominator, its inverse and the lse
+            const float l = (sm.lpart[0][h] + sm.lpart[1][h]) + (sm.lpart[2][h] + sm.lpart[3][h]);
+            sm.inv_l[h] = l > 0.f ? 1.0f / l : 0.f;
+            const float lse = l > 0.f ? (m_run + log2f(l)) * LN2 : -INFINITY;
+            if (p.splits == 1) {
+                if (p.lse) p.lse[(size_t)it.bm * NH + h] = lse;
+            } else {
+                p.lse_part[(size_t)it.split * rows + (size_t)it.bm * NH + h] = lse;
+            }
+        }
         tc_fence_after();
         uint32_t ov[32];
         tmem_ld32(t_o, ov);
@@ -555,23 +645,21 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
+        softmax_sync_or(slot, 0);  // inv_l complete
         // O / l straight from registers: for each head the 128 threads of the
         // group write 128 consecutive values of d (coalesced)
         const int d = quarter * 32 + lane;
-        const size_t rows = (size_t)p.B * p.M * NH;
         if (p.splits == 1) {
             __nv_bfloat16 *ob = p.o + (size_t)it.bm * NH * HD + d;
 #pragma unroll
             for (int hh = 0; hh < NH; ++hh)
-                ob[hh * HD] = __float2bfloat16_rn(__uint_as_float(ov[hh]) * sm.l[hh]);
-            if (p.lse && tid < NH) p.lse[(size_t)it.bm * NH + tid] = sm.m[tid];
+                ob[hh * HD] = __float2bfloat16_rn(__uint_as_float(ov[hh]) * sm.inv_l[hh]);
         } else {
             float *op = p.o_part + ((size_t)it.split * rows + (size_t)it.bm * NH) * HD + d;
 #pragma unroll
-            for (int hh = 0; hh < NH; ++hh) op[hh * HD] = __uint_as_float(ov[hh]) * sm.l[hh];
-            if (tid < NH) p.lse_part[(size_t)it.split * rows + (size_t)it.bm * NH + tid] = sm.m[tid];
+            for (int hh = 0; hh < NH; ++hh) op[hh * HD] = __uint_as_float(ov[hh]) * sm.inv_l[hh];
         }
-        // sm.l / sm.m are rewritten only after two more barriers
+        // lpart / inv_l are rewritten only after the next item's barriers
     }
 }
 
@@ -595,6 +683,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const
                 mbar_init(smem_u32(&b.p_full[i]), 4);
                 mbar_init(smem_u32(&b.p_empty[i]), 1);
             }
+            for (int i = 0; i < IDX_RING; ++i) mbar_init(smem_u32(&b.idx_ready[i]), 1);
             mbar_init(smem_u32(&b.q_full), 1);
             mbar_init(smem_u32(&b.q_empty), 1);
             mbar_init(smem_u32(&b.pv_done), 1);
@@ -615,18 +704,19 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const
     // the merge of split partials may be scheduled now; it waits for this
     // grid to finish before reading anything
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // slot s: warps SLOT_CTRL * s + g (gather g), SLOT_CTRL * s + GATHER_WARPS
-    // (MMA), then NSLOT * SLOT_CTRL + 4s .. +3 (softmax: four consecutive warps
-    // cover the four TMEM lane quarters)
+    // slot s: warps SLOT_CTRL * s + role (lead, copy warps, MMA), then
+    // NSLOT * SLOT_CTRL + 4s .. +3 (softmax: four consecutive warps cover the
+    // four TMEM lane quarters)
     const int ctrl = NSLOT * SLOT_CTRL;
     const int slot = warp < ctrl ? warp / SLOT_CTRL : (warp - ctrl) >> 2;
     const uint32_t tmem = all.tmem_base + (uint32_t)slot * SLOT_COLS;
     const int first = blockIdx.x * NSLOT + slot, stride = gridDim.x * NSLOT;
     SlotSmem &sm = all.slot[slot];
     if (warp < ctrl) {
-        const int role = warp % SLOT_CTRL;
-        if (role < GATHER_WARPS) {
-            gather_role(p, &tq, sm, &all.abort, role, first, stride, ctx);
+        const int role = warp % SLOT_CTRL;  // 0 lead, 1 .. GATHER_WARPS copy, then MMA
+        if (role <= GATHER_WARPS) {
+            if (role == 0) gather_lead(p, &tq, sm, &all.abort, first, stride, ctx);
+            else gather_helper(p, sm, &all.abort, role - 1, ctx);
         } else {
             if ((threadIdx.x & 31) == 0) mma_role(p, sm, &all.abort, tmem, first, stride, ctx);
             __syncwarp();
