@@ -90,11 +90,14 @@ struct Bars {
     uint64_t s_full, s_empty, p_full[2], pv_done, o_full, o_empty, drain;
 };
 
-// Operand tiles of one pipeline slot (96 KB).
+// Operand tiles and epilogue staging of one pipeline slot (112 KB).
 struct Slot {
     uint8_t q[Q_TILE];
     uint8_t k[KSTAGES][KV_TILE];
     uint8_t v[VSTAGES][KV_TILE];
+    // epilogue staging: each softmax warp turns its 32 output rows into
+    // whole 128-byte line writes, 128 bytes of every row per pass
+    uint8_t stage[4][32 * 128];
 };
 static_assert(offsetof(Slot, k) % 1024 == 0 && offsetof(Slot, v) % 1024 == 0 &&
                   sizeof(Slot) % 1024 == 0,
@@ -108,6 +111,7 @@ struct Smem {
     uint32_t tmem_base;
     int abort;  // any role that gives up stops every role of the CTA
 };
+static_assert(sizeof(Smem) <= 227 * 1024, "shared memory of one CTA");
 
 struct Item {
     bool valid;
@@ -201,17 +205,15 @@ template <int MODE> struct TileIter {
     }
 };
 
-// K-major operand with 128-byte rows split in 64-column halves `half` bytes
-// apart: descriptor for the kk-th 16-element K slice.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int kk, uint32_t half) {
-    return smem_desc_sw128(base + (uint32_t)(kk >> 2) * half + (uint32_t)(kk & 3) * 32u, 16u,
-                           1024u);
+// Shared-memory descriptors are built once per buffer; the K step kk (16
+// elements) only moves the start address, whose field holds address >> 4 in
+// the low bits (no carry: shared addresses stay below 256 KB).
+// K-major operand with 128-byte rows split in 64-column halves `half` bytes apart
+__host__ __device__ constexpr uint32_t koff(int kk, uint32_t half) {
+    return ((uint32_t)(kk >> 2) * half + (uint32_t)(kk & 3) * 32u) >> 4;
 }
-// MN-major operand (V: rows = keys, 64-column halves of d KV_HALF bytes apart):
-// descriptor for the kk-th 16-key slice.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
-    return smem_desc_sw128(base + (uint32_t)kk * 2048u, KV_HALF, 1024u);
-}
+// MN-major operand (V: rows = keys, 64-column halves of d KV_HALF bytes apart)
+__host__ __device__ constexpr uint32_t mnoff(int kk) { return (uint32_t)kk * 2048u >> 4; }
 
 constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HD, 0, 1);
@@ -290,8 +292,14 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
                            uint32_t tmem, int first, int stride, const DevCtx &ctx) {
     int qi = 0, kt = 0, pc = 0;
     bool ok = true;
-    const uint32_t q_base = smem_u32(sm.q);
     const uint32_t o_tmem = tmem + O_COL;
+    // descriptors per buffer (two stages each, selected so they stay in registers)
+    static_assert(KSTAGES == 2 && VSTAGES == 2, "descriptor selection assumes two stages");
+    const uint64_t dq = smem_desc_sw128(smem_u32(sm.q), 16u, 1024u);
+    const uint64_t dk0 = smem_desc_sw128(smem_u32(sm.k[0]), 16u, 1024u);
+    const uint64_t dk1 = smem_desc_sw128(smem_u32(sm.k[1]), 16u, 1024u);
+    const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), KV_HALF, 1024u);
+    const uint64_t dv1 = smem_desc_sw128(smem_u32(sm.v[1]), KV_HALF, 1024u);
     for (int v = first; ok && v < p.num_items; v += stride) {
         const Item it = decode_item<MODE>(p, v);
         if (!it.valid || it.ntiles == 0) continue;
@@ -305,12 +313,13 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
                 !mbar_wait(smem_u32(&b.o_empty), (qi - 1) & 1, ctx, abort))
                 return false;
             tc_fence_after();
-            const uint32_t v_base = smem_u32(sm.v[st]);
+            const uint64_t dv = st ? dv1 : dv0;
             const uint32_t p_tmem = tmem + P_COL + 32u * (uint32_t)(pc & 1);
+            const uint32_t acc0 = jj > 0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-                tc_mma_f16_ts(o_tmem, p_tmem + 8u * kk, desc_mnmajor(v_base, kk), IDESC_PV,
-                              (jj > 0 || kk > 0) ? 1u : 0u);
+                tc_mma_f16_ts(o_tmem, p_tmem + 8u * kk, dv + mnoff(kk), IDESC_PV,
+                              kk > 0 ? 1u : acc0);
             tc_commit(smem_u32(&b.v_empty[st]));
             tc_commit(smem_u32(&b.pv_done));
             ++pc;
@@ -323,12 +332,12 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
             if (ok) ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t k_base = smem_u32(sm.k[st]);
+            const uint64_t dk = st ? dk1 : dk0;
             const uint32_t s_tmem = tmem + S_COL;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
-                tc_mma_f16(s_tmem, desc_kmajor(q_base, kk, Q_HALF), desc_kmajor(k_base, kk, KV_HALF),
-                           IDESC_S, kk > 0 ? 1u : 0u);
+                tc_mma_f16(s_tmem, dq + koff(kk, Q_HALF), dk + koff(kk, KV_HALF), IDESC_S,
+                           kk > 0 ? 1u : 0u);
             tc_commit(smem_u32(&b.k_empty[st]));
             tc_commit(smem_u32(&b.s_full));
             if (j == n - 1) tc_commit(smem_u32(&b.q_empty));
@@ -348,8 +357,8 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
 // ------------------------------------------------------------------ softmax / epilogue
 
 template <int MODE>
-__device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, uint32_t tmem,
-                             int first, int stride, const DevCtx &ctx) {
+__device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile int *abort,
+                             uint32_t tmem, int first, int stride, const DevCtx &ctx) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
@@ -525,39 +534,62 @@ __device__ void softmax_role(const TcParams &p, Bars &b, volatile int *abort, ui
         tc_fence_after();
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const size_t orow = (size_t)(it.q_row0 + r) * p.H + it.h;
+        // Each pass covers 128 bytes of every row: this thread's row goes to
+        // the warp's staging buffer (128B-swizzled, conflict-free), then the
+        // warp writes 4 whole rows (4 lines) per store instruction.
+        {
+            const uint32_t sb = smem_u32(slot.stage[quarter]);
+            constexpr int PASSES = MODE == MODE_WINDOW ? 2 : 4;  // bf16: 64 d, fp32: 32 d per pass
+            constexpr int ROW_BYTES = MODE == MODE_WINDOW ? HD * 2 : HD * 4;
+            uint8_t *const obase = MODE == MODE_WINDOW ? reinterpret_cast<uint8_t *>(p.o)
+                                                       : reinterpret_cast<uint8_t *>(p.o_part);
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-            uint32_t ov[2][32];
-            tmem_ld32(o_tmem + 64u * half, ov[0]);
-            tmem_ld32(o_tmem + 64u * half + 32u, ov[1]);
-            tc_wait_ld();
-            if (half == 1) {  // O fully read: the next item's first P V may overwrite it
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
-            }
-            if (!row_valid) continue;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * half + cc;
+            for (int pass = 0; pass < PASSES; ++pass) {
+                uint32_t w[32];  // this row's 128 bytes
                 if (MODE == MODE_WINDOW) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + orow * HD + 32 * c);
+                    uint32_t ov[2][32];
+                    tmem_ld32(o_tmem + 64u * pass, ov[0]);
+                    tmem_ld32(o_tmem + 64u * pass + 32u, ov[1]);
+                    tc_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 0]) * inv, __uint_as_float(ov[cc][8 * u + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 2]) * inv, __uint_as_float(ov[cc][8 * u + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 4]) * inv, __uint_as_float(ov[cc][8 * u + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(ov[cc][8 * u + 6]) * inv, __uint_as_float(ov[cc][8 * u + 7]) * inv);
-                        dst[u] = w;
-                    }
+                    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[16 * cc + e] = pack_bf16x2(__uint_as_float(ov[cc][2 * e]) * inv,
+                                                         __uint_as_float(ov[cc][2 * e + 1]) * inv);
                 } else {
-                    float4 *dst = reinterpret_cast<float4 *>(p.o_part + orow * HD + 32 * c);
+                    uint32_t ov[32];
+                    tmem_ld32(o_tmem + 32u * pass, ov);
+                    tc_wait_ld();
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        dst[u] = make_float4(__uint_as_float(ov[cc][4 * u]) * inv, __uint_as_float(ov[cc][4 * u + 1]) * inv,
-                                             __uint_as_float(ov[cc][4 * u + 2]) * inv, __uint_as_float(ov[cc][4 * u + 3]) * inv);
+                    for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(ov[e]) * inv);
                 }
+                if (pass == PASSES - 1) {  // O fully read: the next item's first P V may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     sb + (uint32_t)lane * 128u + (((uint32_t)u ^ (lane & 7u)) << 4)),
+                                 "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                                 : "memory");
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rw = 4 * i + (lane >> 3), unit = lane & 7;  // row in the warp, 16-B unit
+                    uint4 v;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                 : "r"(sb + (uint32_t)rw * 128u + (((uint32_t)unit ^ ((uint32_t)rw & 7u)) << 4)));
+                    const int rr = quarter * 32 + rw;
+                    if (rr < it.nq) {
+                        const size_t grow = (size_t)(it.q_row0 + rr) * p.H + it.h;
+                        *reinterpret_cast<uint4 *>(obase + grow * ROW_BYTES + pass * 128 + unit * 16) = v;
+                    }
+                }
+                __syncwarp();  // the buffer is rewritten by the next pass
             }
         }
         if (row_valid) {
@@ -632,7 +664,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         }
         __syncwarp();
     } else {
-        softmax_role<MODE>(p, sm.bars[slot], &sm.abort, tmem, first, stride, ctx);
+        softmax_role<MODE>(p, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride, ctx);
     }
     tc_fence_before();
     __syncthreads();

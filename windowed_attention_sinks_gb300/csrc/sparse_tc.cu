@@ -119,13 +119,18 @@ struct SpParams {
 constexpr uint32_t IDESC_S = idesc_bf16_f32(128, NH, 0, 0);
 constexpr uint32_t IDESC_O = idesc_bf16_f32(128, NH, 1, 0);
 
-__device__ __forceinline__ uint64_t desc_k(uint32_t base, int kk, uint32_t half_stride) {
-    return smem_desc_sw128(base + (uint32_t)(kk >> 2) * half_stride + (uint32_t)(kk & 3) * 32u,
-                           16u, 1024u);
+// Shared-memory descriptors are built once per buffer; the K step kk (16
+// elements) only moves the start address, whose field holds address >> 4 in
+// the low bits (no carry: shared addresses stay below 256 KB).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t base, uint32_t lbo) {
+    return smem_desc_sw128(base, lbo, 1024u);
 }
-__device__ __forceinline__ uint64_t desc_mn(uint32_t base, int kk) {
-    return smem_desc_sw128(base + (uint32_t)kk * 2048u, KV_HALF, 1024u);
+// K-major operand split in 64-element halves `half_stride` bytes apart
+__host__ __device__ constexpr uint32_t koff(int kk, uint32_t half_stride) {
+    return ((uint32_t)(kk >> 2) * half_stride + (uint32_t)(kk & 3) * 32u) >> 4;
 }
+// MN-major operand: 16 K rows of 128 bytes per step
+__host__ __device__ constexpr uint32_t mnoff(int kk) { return (uint32_t)kk * 2048u >> 4; }
 
 // 2-D tiled TMA load (x = column, y = row), completion on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
@@ -378,7 +383,15 @@ __device__ void mma_role(const SpParams &p, SlotSmem &sm, volatile int *abort, u
     SlotBars &b = sm.b;
     const int nitems = p.B * p.M * p.splits;
     const int my_items = first < nitems ? (nitems - first + stride - 1) / stride : 0;
-    const uint32_t q_base = smem_u32(sm.q), t_o = tmem + O_COL;
+    const uint32_t t_o = tmem + O_COL;
+    const uint64_t dq = desc_sw128(smem_u32(sm.q), 16u);
+    // per stage (selected, not indexed, so that they stay in registers)
+    const uint64_t dkv0 = desc_sw128(smem_u32(sm.kv[0]), 16u);
+    const uint64_t dkv1 = desc_sw128(smem_u32(sm.kv[1]), 16u);
+    const uint64_t dmn0 = desc_sw128(smem_u32(sm.kv[0]), KV_HALF);
+    const uint64_t dmn1 = desc_sw128(smem_u32(sm.kv[1]), KV_HALF);
+    const uint64_t dp0 = desc_sw128(smem_u32(sm.p[0]), 16u);
+    const uint64_t dp1 = desc_sw128(smem_u32(sm.p[1]), 16u);
     int s_t = 0, s_item = 0;     // next tile / item for S
     int pv_t = 0, pv_item = 0;   // next tile / item for P V
     bool s_first = true, pv_first = true;  // the next tile opens its item
@@ -394,11 +407,11 @@ __device__ void mma_role(const SpParams &p, SlotSmem &sm, volatile int *abort, u
                 mbar_try_wait(smem_u32(&b.kv_full[st]), use & 1)) {
                 tc_fence_after();
                 const bool last = sm.tile_last[s_t % IDX_RING] != 0;
-                const uint32_t kv_s = smem_u32(sm.kv[st]);
+                const uint64_t a = st ? dkv1 : dkv0;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
-                    tc_mma_f16(tmem + S_COL + 32u * st, desc_k(kv_s, kk, KV_HALF),
-                               desc_k(q_base, kk, QP_HALF), IDESC_S, kk > 0 ? 1u : 0u);
+                    tc_mma_f16(tmem + S_COL + 32u * st, a + koff(kk, KV_HALF),
+                               dq + koff(kk, QP_HALF), IDESC_S, kk > 0 ? 1u : 0u);
                 tc_commit(smem_u32(&b.s_full[st]));
                 if (last) {
                     tc_commit(smem_u32(&b.q_empty));
@@ -418,11 +431,12 @@ __device__ void mma_role(const SpParams &p, SlotSmem &sm, volatile int *abort, u
                 (!pv_first || pv_item == 0 ||
                  mbar_try_wait(smem_u32(&b.o_empty), (pv_item - 1) & 1))) {
                 tc_fence_after();
-                const uint32_t kv_s = smem_u32(sm.kv[st]), p_s = smem_u32(sm.p[st]);
+                const uint64_t a = st ? dmn1 : dmn0, bp = st ? dp1 : dp0;
+                const uint32_t acc0 = pv_first ? 0u : 1u;
 #pragma unroll
                 for (int kk = 0; kk < R / 16; ++kk)
-                    tc_mma_f16(t_o, desc_mn(kv_s, kk), desc_k(p_s, kk, QP_HALF), IDESC_O,
-                               (!pv_first || kk > 0) ? 1u : 0u);
+                    tc_mma_f16(t_o, a + mnoff(kk), bp + koff(kk, QP_HALF), IDESC_O,
+                               kk > 0 ? 1u : acc0);
                 tc_commit(smem_u32(&b.kv_empty[st]));
                 tc_commit(smem_u32(&b.p_empty[st]));
                 tc_commit(smem_u32(&b.pv_done));
