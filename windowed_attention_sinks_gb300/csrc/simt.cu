@@ -209,14 +209,33 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(MergeArgs a) {
     z = warp_sum(z);
     if (a.sinks) z += ex2((sink - m) * LOG2E);
     const float L = m + logf(z);
-    for (int e = lane; e < a.d; e += 32) {
-        float acc = 0.0f;
+    if (a.d <= 128) {
+        // up to four columns per lane (lane, lane+32, ...), accumulated over
+        // the splits; loads of different splits are independent
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
         for (int c = 0; c < a.C; ++c) {
             const float lc = __ldg(a.lse_parts + (int64_t)c * a.R + r);
-            if (lc == -INFINITY) continue;
-            acc += ex2((lc - L) * LOG2E) * __ldg(a.o_parts + ((int64_t)c * a.R + r) * a.d + e);
+            if (lc == -INFINITY) continue;  // the same for every lane
+            const float w = ex2((lc - L) * LOG2E);
+            const float *src = a.o_parts + ((int64_t)c * a.R + r) * a.d;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (lane + 32 * k < a.d) acc[k] += w * __ldg(src + lane + 32 * k);
         }
-        orow[e] = from_f32<TO>(acc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (lane + 32 * k < a.d) orow[lane + 32 * k] = from_f32<TO>(acc[k]);
+    } else {
+        for (int e = lane; e < a.d; e += 32) {
+            float acc = 0.0f;
+            for (int c = 0; c < a.C; ++c) {
+                const float lc = __ldg(a.lse_parts + (int64_t)c * a.R + r);
+                if (lc == -INFINITY) continue;
+                acc += ex2((lc - L) * LOG2E) * __ldg(a.o_parts + ((int64_t)c * a.R + r) * a.d + e);
+            }
+            orow[e] = from_f32<TO>(acc);
+        }
     }
     if (a.lse && lane == 0) a.lse[r] = L;
 }
