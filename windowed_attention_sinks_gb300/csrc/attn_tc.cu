@@ -19,7 +19,9 @@
 //                 columns), then O += P V into TMEM with P read from TMEM
 //                 (A operand in tensor memory, two P buffers of 32 columns).
 //   warps 4+4s..  softmax + epilogue (four warps): thread = query row = TMEM lane. Each
-//                 row keeps its running max m and sum l in the log2 domain.
+//                 row keeps its running max m and sum l in the log2 domain. An item's
+//                 epilogue runs after the first tile of the next item, so the
+//                 softmax is busy while the item's last P V drains.
 // S of tile j+1 is computed as soon as the softmax has loaded S of tile j.
 // No tensor-memory column is read by one MMA and written by a later one, so
 // ordering rests only on commits and barriers; since S of tile j is issued
@@ -366,6 +368,88 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
     const uint32_t o_tmem = tmem + O_COL + lane_off;
     int sc = 0, pc = 0, qi = 0;  // sc: tiles seen, pc: P tiles written
     bool ok = true;
+    // The epilogue of an item runs after the first tile of the next one: the
+    // softmax works on that tile while the item's last P V drains.
+    struct Pend {
+        bool valid;
+        int q_row0, nq, h;
+        float m, l;
+    };
+    Pend pend{false, 0, 0, 0, 0.f, 0.f};
+    auto epilogue = [&](const Pend &pe) -> bool {
+        if (!mbar_wait(smem_u32(&b.o_full), qi & 1, ctx, abort)) return false;
+        tc_fence_after();
+        const float inv = pe.l > 0.0f ? 1.0f / pe.l : 0.0f;
+        const size_t orow = (size_t)(pe.q_row0 + r) * p.H + pe.h;
+        // Each pass covers 128 bytes of every row: this thread's row goes to
+        // the warp's staging buffer (128B-swizzled, conflict-free), then the
+        // warp writes 4 whole rows (4 lines) per store instruction.
+        {
+            const uint32_t sb = smem_u32(slot.stage[quarter]);
+            constexpr int PASSES = MODE == MODE_WINDOW ? 2 : 4;  // bf16: 64 d, fp32: 32 d per pass
+            constexpr int ROW_BYTES = MODE == MODE_WINDOW ? HD * 2 : HD * 4;
+            uint8_t *const obase = MODE == MODE_WINDOW ? reinterpret_cast<uint8_t *>(p.o)
+                                                       : reinterpret_cast<uint8_t *>(p.o_part);
+#pragma unroll 1
+            for (int pass = 0; pass < PASSES; ++pass) {
+                uint32_t w[32];  // this row's 128 bytes
+                if (MODE == MODE_WINDOW) {
+                    uint32_t ov[2][32];
+                    tmem_ld32(o_tmem + 64u * pass, ov[0]);
+                    tmem_ld32(o_tmem + 64u * pass + 32u, ov[1]);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[16 * cc + e] = pack_bf16x2(__uint_as_float(ov[cc][2 * e]) * inv,
+                                                         __uint_as_float(ov[cc][2 * e + 1]) * inv);
+                } else {
+                    uint32_t ov[32];
+                    tmem_ld32(o_tmem + 32u * pass, ov);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(ov[e]) * inv);
+                }
+                if (pass == PASSES - 1) {  // O fully read: the next item's first P V may overwrite it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                     sb + (uint32_t)lane * 128u + (((uint32_t)u ^ (lane & 7u)) << 4)),
+                                 "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
+                                 : "memory");
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rw = 4 * i + (lane >> 3), unit = lane & 7;  // row in the warp, 16-B unit
+                    uint4 v;
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                                 : "r"(sb + (uint32_t)rw * 128u + (((uint32_t)unit ^ ((uint32_t)rw & 7u)) << 4)));
+                    const int rr = quarter * 32 + rw;
+                    if (rr < pe.nq) {
+                        const size_t grow = (size_t)(pe.q_row0 + rr) * p.H + pe.h;
+                        *reinterpret_cast<uint4 *>(obase + grow * ROW_BYTES + pass * 128 + unit * 16) = v;
+                    }
+                }
+                __syncwarp();  // the buffer is rewritten by the next pass
+            }
+        }
+        if (r < pe.nq) {
+            const float lse = pe.l > 0.0f ? (pe.m + log2f(pe.l)) * LN2 : -INFINITY;
+            if (MODE == MODE_WINDOW) {
+                if (p.lse) p.lse[orow] = lse;
+            } else {
+                p.lse_part[orow] = lse;
+            }
+        }
+        ++qi;
+        return true;
+    };
     for (int v = first; ok && v < p.num_items; v += stride) {
         const Item it = decode_item<MODE>(p, v);
         if (!it.valid) {
@@ -527,81 +611,15 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&b.p_full[pc & 1]));
             ++pc;
+            if (j == 0 && pend.valid) {
+                if (!(ok = epilogue(pend))) break;
+                pend.valid = false;
+            }
         }
         if (!ok) break;
-        // epilogue: O / l -> global, lse
-        if (!mbar_wait(smem_u32(&b.o_full), qi & 1, ctx, abort)) { ok = false; break; }
-        tc_fence_after();
-        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const size_t orow = (size_t)(it.q_row0 + r) * p.H + it.h;
-        // Each pass covers 128 bytes of every row: this thread's row goes to
-        // the warp's staging buffer (128B-swizzled, conflict-free), then the
-        // warp writes 4 whole rows (4 lines) per store instruction.
-        {
-            const uint32_t sb = smem_u32(slot.stage[quarter]);
-            constexpr int PASSES = MODE == MODE_WINDOW ? 2 : 4;  // bf16: 64 d, fp32: 32 d per pass
-            constexpr int ROW_BYTES = MODE == MODE_WINDOW ? HD * 2 : HD * 4;
-            uint8_t *const obase = MODE == MODE_WINDOW ? reinterpret_cast<uint8_t *>(p.o)
-                                                       : reinterpret_cast<uint8_t *>(p.o_part);
-#pragma unroll 1
-            for (int pass = 0; pass < PASSES; ++pass) {
-                uint32_t w[32];  // this row's 128 bytes
-                if (MODE == MODE_WINDOW) {
-                    uint32_t ov[2][32];
-                    tmem_ld32(o_tmem + 64u * pass, ov[0]);
-                    tmem_ld32(o_tmem + 64u * pass + 32u, ov[1]);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            w[16 * cc + e] = pack_bf16x2(__uint_as_float(ov[cc][2 * e]) * inv,
-                                                         __uint_as_float(ov[cc][2 * e + 1]) * inv);
-                } else {
-                    uint32_t ov[32];
-                    tmem_ld32(o_tmem + 32u * pass, ov);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) w[e] = __float_as_uint(__uint_as_float(ov[e]) * inv);
-                }
-                if (pass == PASSES - 1) {  // O fully read: the next item's first P V may overwrite it
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                                     sb + (uint32_t)lane * 128u + (((uint32_t)u ^ (lane & 7u)) << 4)),
-                                 "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
-                                 : "memory");
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rw = 4 * i + (lane >> 3), unit = lane & 7;  // row in the warp, 16-B unit
-                    uint4 v;
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                                 : "r"(sb + (uint32_t)rw * 128u + (((uint32_t)unit ^ ((uint32_t)rw & 7u)) << 4)));
-                    const int rr = quarter * 32 + rw;
-                    if (rr < it.nq) {
-                        const size_t grow = (size_t)(it.q_row0 + rr) * p.H + it.h;
-                        *reinterpret_cast<uint4 *>(obase + grow * ROW_BYTES + pass * 128 + unit * 16) = v;
-                    }
-                }
-                __syncwarp();  // the buffer is rewritten by the next pass
-            }
-        }
-        if (row_valid) {
-            const float lse = l > 0.0f ? (m_run + log2f(l)) * LN2 : -INFINITY;
-            if (MODE == MODE_WINDOW) {
-                if (p.lse) p.lse[orow] = lse;
-            } else {
-                p.lse_part[orow] = lse;
-            }
-        }
-        ++qi;
+        pend = Pend{true, it.q_row0, it.nq, it.h, m_run, l};
     }
+    if (ok && pend.valid) epilogue(pend);
 }
 
 template <int MODE>
