@@ -64,6 +64,7 @@ constexpr uint32_t S_COL = 0, P_COL = 64;
 constexpr uint32_t TMEM_COLS = SLOT_COLS * NSLOTS;
 constexpr uint32_t O_COL = 128;
 constexpr float TAU = 8.0f;               // rescale threshold (log2 units)
+constexpr int ITEM_RING = 4;              // items the producer may hand on ahead
 constexpr unsigned FULL = 0xffffffffu;
 
 enum : int { MODE_WINDOW = 0, MODE_BLOCK = 1 };
@@ -83,6 +84,7 @@ struct TcParams {
     const uint8_t *mask;
     int M, Nctx, q_pos0, kv_begin, kv_end, QB, KB;
     float *o_part, *lse_part;
+    unsigned *work;  // zeroed per launch: next item to claim
 };
 
 struct Bars {
@@ -90,6 +92,9 @@ struct Bars {
     // p_full is per P buffer: a softmax warp may run one tile ahead of the
     // others, so arrivals for consecutive tiles must not share a barrier.
     uint64_t s_full, s_empty, p_full[2], pv_done, o_full, o_empty, drain;
+    // items claimed by the producer, handed to the MMA issuer and softmax warps
+    uint64_t item_full[ITEM_RING], item_empty[ITEM_RING];
+    int item[ITEM_RING];  // item index, or -1: no more items
 };
 
 // Operand tiles and epilogue staging of one pipeline slot (112 KB).
@@ -256,9 +261,51 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
         return true;
     };
     bool ok = true;
-    for (int v = first; ok && v < p.num_items; v += stride) {
+    // Items are claimed from the launch's counter (the slot that frees up first
+    // takes the next one) and handed on through the item ring; items past the
+    // end of a short sequence are skipped here and never reach the others.
+    int ip = 0;  // items published
+    auto publish = [&](int v) -> bool {
+        const int k = ip % ITEM_RING, use = ip / ITEM_RING;
+        if (use >= 1 && !mbar_wait(smem_u32(&b.item_empty[k]), (use - 1) & 1, ctx, abort))
+            return false;
+        b.item[k] = v;
+        mbar_arrive(smem_u32(&b.item_full[k]));
+        ++ip;
+        return true;
+    };
+    // Item order. Window mode: the first 7/8 of the item range is dealt out
+    // round-robin (item first + k * stride): the slots of the grid then work on
+    // neighbouring query tiles and adjacent heads at the same time, which share
+    // K/V bands in L2 and token rows in HBM. The rest is claimed one item at a
+    // time from the launch's counter, so that slots that finish early take the
+    // remaining work. Block mode (few items per slot) claims every item.
+    const int v_static =
+        MODE == MODE_WINDOW ? (p.num_items / 8 * 7 / stride) * stride : 0;
+    int v_next = first;  // next round-robin item
+    for (;;) {
+        int v;
+        if (v_next < v_static) {
+            v = v_next;
+            v_next += stride;
+        } else {
+            v = v_static + (int)atomicAdd(p.work, 1u);
+            if (v >= p.num_items) break;
+        }
         const Item it = decode_item<MODE>(p, v);
-        if (!it.valid || it.ntiles == 0) continue;
+        if (!it.valid) {
+            if (it.seq_err) {
+                record_error(ctx, DEVERR_SEQLENS);
+            } else if (MODE == MODE_WINDOW && v >= v_static) {
+                // every later item of this sequence lies past its end as well:
+                // move the counter to the next sequence's first item
+                const int per_seq = p.H * p.tiles_per_seq;
+                atomicMax(p.work, (unsigned)((v / per_seq + 1) * per_seq - v_static));
+            }
+            continue;
+        }
+        if (!(ok = publish(v))) break;
+        if (it.ntiles == 0) continue;
         if (qi >= 1) ok = mbar_wait(smem_u32(&b.q_empty), (qi - 1) & 1, ctx, abort);
         if (!ok) break;
         const uint32_t qbar = smem_u32(&b.q_full);
@@ -275,7 +322,9 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
             prev_row = row;
         }
         if (ok) ok = load_v(it.g, prev_row);
+        if (!ok) break;
     }
+    if (ok) ok = publish(-1);
     if (!ok) {
         // Let copies already in flight land before the CTA leaves (bounded).
         int zero = 0;
@@ -302,9 +351,14 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
     const uint64_t dk1 = smem_desc_sw128(smem_u32(sm.k[1]), 16u, 1024u);
     const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), KV_HALF, 1024u);
     const uint64_t dv1 = smem_desc_sw128(smem_u32(sm.v[1]), KV_HALF, 1024u);
-    for (int v = first; ok && v < p.num_items; v += stride) {
+    for (int ic = 0; ok; ++ic) {
+        const int slot_k = ic % ITEM_RING;
+        if (!mbar_wait(smem_u32(&b.item_full[slot_k]), (ic / ITEM_RING) & 1, ctx, abort)) break;
+        const int v = b.item[slot_k];
+        mbar_arrive(smem_u32(&b.item_empty[slot_k]));
+        if (v < 0) break;
         const Item it = decode_item<MODE>(p, v);
-        if (!it.valid || it.ntiles == 0) continue;
+        if (it.ntiles == 0) continue;
         ok = mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort);
         const int n = it.ntiles, kt0 = kt;
         auto issue_pv = [&](int jj) -> bool {
@@ -450,12 +504,17 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
         ++qi;
         return true;
     };
-    for (int v = first; ok && v < p.num_items; v += stride) {
-        const Item it = decode_item<MODE>(p, v);
-        if (!it.valid) {
-            if (it.seq_err && quarter == 0 && lane == 0) record_error(ctx, DEVERR_SEQLENS);
-            continue;
+    for (int ic = 0; ok; ++ic) {
+        const int slot_k = ic % ITEM_RING;
+        if (!mbar_wait(smem_u32(&b.item_full[slot_k]), (ic / ITEM_RING) & 1, ctx, abort)) {
+            ok = false;
+            break;
         }
+        const int v = b.item[slot_k];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&b.item_empty[slot_k]));
+        if (v < 0) break;
+        const Item it = decode_item<MODE>(p, v);
         const bool row_valid = r < it.nq;
         if (it.ntiles == 0) {  // block mode: nothing visible in this chunk
             if (MODE == MODE_BLOCK && row_valid) {
@@ -656,6 +715,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
             mbar_init(smem_u32(&b.o_full), 1);
             mbar_init(smem_u32(&b.o_empty), 4);
             mbar_init(smem_u32(&b.drain), 1);
+            for (int i = 0; i < ITEM_RING; ++i) {
+                mbar_init(smem_u32(&b.item_full[i]), 1);
+                mbar_init(smem_u32(&b.item_empty[i]), 1 + 4);  // MMA issuer + softmax warps
+            }
         }
         sm.abort = 0;
         fence_mbar_init();
@@ -702,9 +765,10 @@ CUresult make_map(CUtensorMap *m, const void *base, int rows, int heads, uint32_
                              strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int MODE> cudaError_t launch(const TcParams &p, const void *q, int q_rows,
+template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int q_rows,
                                        const void *k, const void *v, int kv_rows,
                                        const DevInfo &dev, cudaStream_t s) {
+    TcParams p = p_in;
     for (const void *ptr : {q, k, v})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return cudaErrorMisalignedAddress;
     CUtensorMap tq, tk, tv;
@@ -721,6 +785,8 @@ template <int MODE> cudaError_t launch(const TcParams &p, const void *q, int q_r
     }
     const int streams = (p.num_items + NSLOTS - 1) / NSLOTS;
     const int grid = streams < dev.sm_count ? streams : dev.sm_count;
+    cudaError_t e;
+    if (!(p.work = work_counter(dev, s, &e))) return e;
     DevCtx ctx{dev.err, wait_limit_ns()};
     if (verbose())
         fprintf(stderr, "sattn: attn_tc_kernel<%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",

@@ -15,12 +15,18 @@ struct DevInfo {
     int device = -1;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
-    unsigned *err = nullptr;  // device address of the error word
+    unsigned *err = nullptr;       // device address of the error word
+    unsigned *counters = nullptr;  // device address of the work-counter slots
 };
 
 // Per-device facts, initialised once per device (thread-safe).
 const DevInfo *device_info(cudaError_t *e);
 uint64_t wait_limit_ns();
+// A zeroed work counter for one launch on `s`: the next of a ring of slots
+// (each on its own 128-byte line), cleared by an asynchronous memset on `s`,
+// so launches on different streams do not share a counter. Returns nullptr
+// (and sets *e) if the memset cannot be issued.
+unsigned *work_counter(const DevInfo &dev, cudaStream_t s, cudaError_t *e);
 // True when the environment variable SATTN_VERBOSE is set (launch reports on stderr).
 bool verbose();
 
