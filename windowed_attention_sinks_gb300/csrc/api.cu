@@ -15,10 +15,10 @@
 namespace sattn {
 
 __device__ unsigned g_error_word;
-// Per-launch work counters of the persistent kernels (dynamic item order):
-// a ring of slots, one 128-byte line each.
-constexpr unsigned kCounterSlots = 256, kCounterStride = 32;
-__device__ unsigned g_work_counters[kCounterSlots * kCounterStride];
+// Per-launch counters of the persistent kernels (claimed items, arrivals of
+// split partials): a ring of blocks, each cleared on the launch's stream.
+constexpr unsigned kCounterBlocks = 64;
+__device__ unsigned g_counters[kCounterBlocks * kCounterBlock];
 
 namespace {
 
@@ -77,7 +77,7 @@ const DevInfo *device_info(cudaError_t *e) {
         void *p = nullptr;
         if ((*e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return nullptr;
         d.err = static_cast<unsigned *>(p);
-        if ((*e = cudaGetSymbolAddress(&p, g_work_counters)) != cudaSuccess) return nullptr;
+        if ((*e = cudaGetSymbolAddress(&p, g_counters)) != cudaSuccess) return nullptr;
         d.counters = static_cast<unsigned *>(p);
         if ((*e = cudaMemset(d.err, 0, sizeof(unsigned))) != cudaSuccess) return nullptr;
         if ((*e = cudaDeviceSynchronize()) != cudaSuccess) return nullptr;
@@ -89,10 +89,14 @@ const DevInfo *device_info(cudaError_t *e) {
 
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
-unsigned *work_counter(const DevInfo &dev, cudaStream_t s, cudaError_t *e) {
+unsigned *launch_counters(const DevInfo &dev, cudaStream_t s, unsigned n, cudaError_t *e) {
+    if (n == 0 || n > kCounterBlock) {
+        *e = cudaErrorInvalidValue;
+        return nullptr;
+    }
     static std::atomic<unsigned> next{0};
-    unsigned *c = dev.counters + (size_t)(next.fetch_add(1) % kCounterSlots) * kCounterStride;
-    *e = cudaMemsetAsync(c, 0, sizeof(unsigned), s);
+    unsigned *c = dev.counters + (size_t)(next.fetch_add(1) % kCounterBlocks) * kCounterBlock;
+    *e = cudaMemsetAsync(c, 0, n * sizeof(unsigned), s);
     return *e == cudaSuccess ? c : nullptr;
 }
 

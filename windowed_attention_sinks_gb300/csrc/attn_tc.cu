@@ -786,7 +786,7 @@ template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int 
     const int streams = (p.num_items + NSLOTS - 1) / NSLOTS;
     const int grid = streams < dev.sm_count ? streams : dev.sm_count;
     cudaError_t e;
-    if (!(p.work = work_counter(dev, s, &e))) return e;
+    if (!(p.work = launch_counters(dev, s, 1, &e))) return e;
     DevCtx ctx{dev.err, wait_limit_ns()};
     if (verbose())
         fprintf(stderr, "sattn: attn_tc_kernel<%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",

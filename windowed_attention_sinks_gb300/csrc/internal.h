@@ -16,17 +16,19 @@ struct DevInfo {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned *err = nullptr;       // device address of the error word
-    unsigned *counters = nullptr;  // device address of the work-counter slots
+    unsigned *counters = nullptr;  // device address of the per-launch counter blocks
 };
 
 // Per-device facts, initialised once per device (thread-safe).
 const DevInfo *device_info(cudaError_t *e);
 uint64_t wait_limit_ns();
-// A zeroed work counter for one launch on `s`: the next of a ring of slots
-// (each on its own 128-byte line), cleared by an asynchronous memset on `s`,
-// so launches on different streams do not share a counter. Returns nullptr
-// (and sets *e) if the memset cannot be issued.
-unsigned *work_counter(const DevInfo &dev, cudaStream_t s, cudaError_t *e);
+// n (<= kCounterBlock) zeroed counters for one launch on `s`: the next block
+// of a ring of 64 built into the library, cleared by an asynchronous memset
+// on `s`. A block is reused 64 launches later, so launches on different
+// streams do not share counters unless 64 of them overlap. Returns nullptr
+// (and sets *e) if n is out of range or the memset cannot be issued.
+constexpr unsigned kCounterBlock = 512;
+unsigned *launch_counters(const DevInfo &dev, cudaStream_t s, unsigned n, cudaError_t *e);
 // True when the environment variable SATTN_VERBOSE is set (launch reports on stderr).
 bool verbose();
 
