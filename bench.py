@@ -155,7 +155,7 @@ def run_sattn(args, rank, world, device):
     torch.cuda.set_device(device)
     stream = torch.cuda.current_stream()
     peaks, peaks_src = load_peaks()
-    seed = 1000 + rank  # each rank owns an independent batch (weak scaling)
+    seed = rank_seed(rank)  # each rank owns an independent batch (weak scaling)
     if args.workload != "window":
         return run_other(args, rank, world, device, peaks, peaks_src)
 
@@ -216,7 +216,7 @@ def run_sattn(args, rank, world, device):
     sa.check_device(stream)
 
     ms_per_step = elapsed_ms / args.steps
-    value = total_q * world / (ms_per_step / 1e3)
+    value = whole_job_rate(total_q, world, ms_per_step)
     # Roofline of the dominant launch (Hkv = 16: the most bytes per launch),
     # averaged over its key-0 and null-logit launches.
     lm = np.array(launch_ms)  # [steps, launches]
@@ -344,7 +344,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
 
     stream = torch.cuda.current_stream()
     bf = torch.bfloat16
-    seed = 1000 + rank
+    seed = rank_seed(rank)
     if args.workload in ("decode", "prefill"):
         case = W.sparse_decode_bf16(seed) if args.workload == "decode" else \
             W.sparse_prefill_bf16(seed)
@@ -433,7 +433,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
     tf = flops / (ms / 1e3) / 1e12
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     return {
-        "metric": "queries/s (%s)" % args.workload, "value": units * world / (ms / 1e3),
+        "metric": "queries/s (%s)" % args.workload, "value": whole_job_rate(units, world, ms),
         "unit": "queries/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded numpy PCG64, bf16)",
@@ -513,9 +513,21 @@ def max_over_ranks(x, world):
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seed(rank):
+    """Seed of the batch rank `rank` owns: every rank runs an independent batch of
+    the same shape (weak scaling, no data-path collective)."""
+    return 1000 + rank
+
+
+def whole_job_rate(units_per_rank, world, ms_max):
+    """Units all ranks processed per second, over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
 
 
 def gpu_index(device):
