@@ -5,8 +5,9 @@ benchmark's CPU-baseline leg are the only callers. The library path never
 imports this package. The C source (`sattn_oracle.c`) shares nothing with the
 CUDA implementation.
 
-The functions take float32 numpy arrays (the exact input values, bf16 inputs
-widened) and return float64 outputs. Each accepts an optional `rows` array of
+The attention functions take float32 numpy arrays (the exact input values,
+bf16 inputs widened) and return float64 outputs; `topk_idxs` and
+`kv_ring_write` (cache bookkeeping around the path) are plain Python. Each accepts an optional `rows` array of
 row ids so that large workloads can be checked on sampled rows:
   window:  row = token * H + head
   sparse:  row = (b * M + m) * H + head
@@ -150,3 +151,63 @@ def merge(o_parts, lse_parts, H, sinks=None):
     lse = np.zeros(R, dtype=np.float64)
     lib.oracle_merge(_ptr(op), _ptr(lp), C, R, d, H, _ptr(s), _ptr(o), _ptr(lse))
     return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Cache bookkeeping around the gathered path ("DeepSeek-V4 CSA/HCA
+# walkthrough", section 2.3 steps 5-6 and section 3.3). Plain Python: these
+# produce integers and copies, so parity with the GPU is exact.
+
+def topk_idxs(start_pos, M, K, win, ratio):
+    """Index lists of M consecutive queries of each request over a
+    [window ring | compressed] cache; returns int32 [B, M, K].
+
+    The query at absolute position p = start_pos[b] + m lists, in order:
+      * the window: the win most recent tokens t = p-win+1 .. p, each at its
+        ring row t mod win (the ring keeps token t in row t mod win), or -1
+        for t < 0;
+      * the compressed rows it may see, c = 0 .. floor(p / ratio) (cache row
+        win + c) in ascending order; when more are visible than the K - win
+        entries left, the most recent ones (no learned indexer here);
+      * -1 for the entries left over. ratio = 0 means no compressed part.
+    """
+    start_pos = np.asarray(start_pos, dtype=np.int64)
+    B = len(start_pos)
+    out = np.full((B, M, K), -1, dtype=np.int32)
+    for b in range(B):
+        for m in range(M):
+            p = int(start_pos[b]) + m
+            entries = []
+            for k in range(win):
+                t = p - win + 1 + k
+                entries.append(t % win if t >= 0 else -1)
+            if ratio > 0:
+                visible = list(range(p // ratio + 1))
+                room = K - win
+                chosen = visible if len(visible) <= room else visible[len(visible) - room:]
+                entries.extend(win + c for c in chosen)
+            n = min(len(entries), K)
+            out[b, m, :n] = entries[:n]
+    return out
+
+
+def kv_ring_write(kv_cache, kv_new, start_pos, win):
+    """Ring write of new KV rows: returns a copy of kv_cache [B, N, d] in which
+    the last min(S, win) of the S new rows of request b (positions
+    start_pos[b] .. start_pos[b] + S - 1) are stored.
+
+    Written as the pages split it: with `cutoff` = the ring row of the first
+    row written, the block goes to rows [cutoff, win) and then wraps to
+    [0, cutoff) (rows before the block's last win are overwritten anyway).
+    """
+    out = np.array(kv_cache, copy=True)
+    kv_new = np.asarray(kv_new)
+    S = kv_new.shape[1]
+    n = min(S, win)
+    for b in range(out.shape[0]):
+        block = kv_new[b, S - n:]
+        cutoff = (int(start_pos[b]) + S - n) % win
+        first = min(win - cutoff, n)
+        out[b, cutoff:cutoff + first] = block[:first]
+        out[b, :n - first] = block[first:]
+    return out
