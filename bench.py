@@ -369,6 +369,25 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                           workspace=ws, stream=st or stream)
         name = "sparse %s bf16: B=%d M=%d H=%d d=%d N=%d K=%d null_logit" % (
             args.workload, case.B, case.M, case.H, case.d, case.N, case.K)
+    elif args.workload == "index":
+        # cache bookkeeping of the prefill layout: index lists of 8192 queries
+        # (K = 2048, window 128, ratio 4) and the ring write of the prompt's KV
+        nb = 0
+        M, K, win, ratio, d = 8192, 2048, 128, 4, 128
+        starts = torch.zeros(1, dtype=torch.int32, device=device)
+        idx_out = torch.empty((1, M, K), dtype=torch.int32, device=device)
+        cache = torch.zeros((1, win + 8192, d), dtype=bf, device=device)
+        new_kv = torch.randn((1, M, d), device=device).to(bf)
+        nbytes = idx_out.numel() * 4 + 2 * win * d * 2
+        flops = 0
+        units = M
+        # the 67 MB of lists fit in L2: a larger scratch is rewritten before each step
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+        def launch(st=None):
+            sa.build_topk_idxs(starts, M, K, win, ratio, out=idx_out, stream=st or stream)
+            sa.kv_ring_write(cache, new_kv, starts, win, stream=st or stream)
+        name = "cache bookkeeping: topk index lists (8192 queries, K=2048, win 128, ratio 4) + ring write"
     else:
         nb = 0
         case = W.block_sparse_bf16(seed)
@@ -401,9 +420,9 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         launch()
     sa.check_device(stream)
     graph = None
-    if args.workload == "decode":
-        # a decode step is ~10 us of device work: it is replayed from a CUDA
-        # graph so that host-side enqueue time stays out of the timed region
+    if args.workload in ("decode", "index"):
+        # a step of ~10-30 us of device work is replayed from a CUDA graph so
+        # that host-side enqueue time stays out of the timed region
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             launch(torch.cuda.current_stream())
@@ -447,7 +466,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                      "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
         # sparse: the gathered-attention kernel, plus the merge when lists are split
         "gpu_launches": args.steps * (len(case.chunks) + 1 if args.workload == "block"
-                                      else (2 if nb > 0 else 1)),
+                                      else 2 if args.workload == "index" or nb > 0 else 1),
         "clocks": clk.summary(),
     }
 
@@ -546,7 +565,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="sattn", choices=["sattn", "reference"])
     ap.add_argument("--workload", default="window", choices=["window", "decode", "prefill",
-                                                              "block"])
+                                                              "block", "index"])
     ap.add_argument("--seqs", type=int, default=256,
                     help="window workload: number of sequences (256 = the full workload)")
     ap.add_argument("--no-e2e", action="store_true")

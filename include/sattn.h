@@ -188,6 +188,48 @@ sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,
                                     int32_t kv_end, int32_t causal, float scale, float *o_part,
                                     float *lse_part, sattn_dtype dtype, void *cuda_stream);
 
+/*
+ * Index lists over a [window ring | compressed] cache ("DeepSeek-V4 CSA/HCA
+ * walkthrough", section 2.3 steps 5-6: the window indices concatenated with
+ * the compressed-region indices form topk_idxs; section 3.3: cache layout
+ * [window_size + max_seq_len / ratio rows], ring row = position mod window).
+ *
+ *   topk_idxs int32 [B, M, K] (device, written), start_pos int32 [B] (device):
+ *   query m of request b sits at absolute position p = start_pos[b] + m and
+ *   lists, in order:
+ *     - win window entries: slot k holds token t = p - win + 1 + k at its
+ *       ring row t mod win, or -1 when t < 0;
+ *     - the compressed rows visible at p, c = 0 .. floor(p / ratio), as cache
+ *       rows win + c in ascending order; when more are visible than the
+ *       K - win entries left, the most recent ones (the pages select these
+ *       with a learned indexer, which is not part of this library);
+ *     - -1 in the entries left over. ratio = 0: no compressed part.
+ * Requirements: B, M, K >= 0, win >= 1, ratio >= 0; positions
+ * start_pos[b] + m in [0, 2^31 - 2] (a query outside that range keeps a list
+ * of -1 and is reported by sattn_check_device as a device check failure).
+ */
+sattn_status sattn_build_topk_idxs(int32_t *topk_idxs, const int32_t *start_pos, int32_t B,
+                                   int32_t M, int32_t K, int32_t win, int32_t ratio,
+                                   void *cuda_stream);
+
+/*
+ * Ring write of new KV rows into the window part of the cache (section 3.3:
+ * the last window_size new rows are stored from row start_pos mod window on,
+ * wrapping to row 0; older rows are overwritten).
+ *
+ *   kv_cache [B, N, d] (dtype, device, updated), kv_new [B, S, d] (dtype,
+ *   device), start_pos int32 [B] (device): the S new rows of request b have
+ *   positions start_pos[b] .. start_pos[b] + S - 1; the last min(S, win) of
+ *   them are stored at rows (position mod win). Rows win .. N-1 (the
+ *   compressed region) are not touched.
+ * Requirements: N >= win >= 1, S >= 0, d * element size a multiple of 16 and
+ * kv_cache, kv_new 16-byte aligned; start_pos[b] >= 0 (a negative entry
+ * writes nothing for that request and is reported by sattn_check_device).
+ */
+sattn_status sattn_kv_ring_write(void *kv_cache, const void *kv_new, const int32_t *start_pos,
+                                 int32_t B, int32_t S, int32_t N, int32_t d, int32_t win,
+                                 sattn_dtype dtype, void *cuda_stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *sattn_status_str(sattn_status s);
 

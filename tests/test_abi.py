@@ -93,6 +93,15 @@ def test_invalid_arguments_rejected_on_host(lib):
                                     fake, fake, 1, None)
     assert rc == 1
     # merge: bad d
+    # index lists: win < 1, negative ratio
+    assert lib.sattn_build_topk_idxs(fake, fake, 1, 4, 16, 0, 4, None) == 1
+    assert lib.sattn_build_topk_idxs(fake, fake, 1, 4, 16, 8, -1, None) == 1
+    assert lib.sattn_build_topk_idxs(None, None, 0, 4, 16, 8, 4, None) == 0  # empty: no work
+    # ring write: N < win, row bytes not a multiple of 16, misaligned pointer
+    assert lib.sattn_kv_ring_write(fake, fake, fake, 1, 4, 4, 128, 8, 1, None) == 1
+    assert lib.sattn_kv_ring_write(fake, fake, fake, 1, 4, 16, 3, 8, 1, None) == 1
+    assert lib.sattn_kv_ring_write(ctypes.c_void_p(fake.value + 4), fake, fake, 1, 4, 16, 128, 8,
+                                   1, None) == 1
     rc = lib.sattn_merge_lse(fake, fake, 2, 10, 0, 8, None, fake, None, 0, None)
     assert rc == 1
 

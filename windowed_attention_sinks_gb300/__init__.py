@@ -56,6 +56,10 @@ def lib() -> ctypes.CDLL:
     L.sattn_block_sparse_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                          f32, P, P, ctypes.c_int, P]
     L.sattn_block_sparse_fwd.restype = ctypes.c_int
+    L.sattn_build_topk_idxs.argtypes = [P, P, i32, i32, i32, i32, i32, P]
+    L.sattn_build_topk_idxs.restype = ctypes.c_int
+    L.sattn_kv_ring_write.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_int, P]
+    L.sattn_kv_ring_write.restype = ctypes.c_int
     L.sattn_status_str.argtypes = [ctypes.c_int]
     L.sattn_status_str.restype = ctypes.c_char_p
     L.sattn_set_debug.argtypes = [ctypes.c_int]
@@ -200,6 +204,38 @@ def block_sparse_fwd(q, k, v, block_mask, q_pos0, kv_begin, kv_end, causal=True,
                                         _dtype_code(q), _stream(stream))
     _check("sattn_block_sparse_fwd", code)
     return o_part, lse_part
+
+
+def build_topk_idxs(start_pos, M, K, win, ratio, out=None, stream=None):
+    """Index lists over a [window ring | compressed] cache (sattn_build_topk_idxs).
+    start_pos: int32 [B] CUDA tensor. Returns int32 [B, M, K]."""
+    import torch
+
+    _need(start_pos, "start_pos", torch.int32)
+    B = start_pos.numel()
+    if out is None:
+        out = torch.empty((B, M, K), dtype=torch.int32, device=start_pos.device)
+    _need(out, "out", torch.int32, start_pos.device)
+    _check("sattn_build_topk_idxs",
+           lib().sattn_build_topk_idxs(_ptr(out), _ptr(start_pos), B, int(M), int(K), int(win),
+                                       int(ratio), _stream(stream)))
+    return out
+
+
+def kv_ring_write(kv_cache, kv_new, start_pos, win, stream=None):
+    """Store the last min(S, win) new rows of each request at their ring rows
+    (sattn_kv_ring_write). kv_cache [B, N, d] is updated in place."""
+    import torch
+
+    B, N, d = kv_cache.shape
+    S = kv_new.shape[1]
+    _need(kv_cache, "kv_cache", None, kv_cache.device)
+    _need(kv_new, "kv_new", kv_cache.dtype, kv_cache.device)
+    _need(start_pos, "start_pos", torch.int32, kv_cache.device)
+    _check("sattn_kv_ring_write",
+           lib().sattn_kv_ring_write(_ptr(kv_cache), _ptr(kv_new), _ptr(start_pos), B, S, N, d,
+                                     int(win), _dtype_code(kv_cache), _stream(stream)))
+    return kv_cache
 
 
 def check_device(stream=None):

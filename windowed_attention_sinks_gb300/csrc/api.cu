@@ -273,6 +273,40 @@ sattn_status sattn_merge_lse(const float *o_parts, const float *lse_parts, int32
     return finish(launch_merge(a, *dev, s), s);
 }
 
+sattn_status sattn_build_topk_idxs(int32_t *topk_idxs, const int32_t *start_pos, int32_t B,
+                                   int32_t M, int32_t K, int32_t win, int32_t ratio,
+                                   void *cuda_stream) {
+    if (B < 0 || M < 0 || K < 0 || win < 1 || ratio < 0) return SATTN_ERR_INVALID_ARG;
+    if ((long long)B * M * K == 0) return SATTN_OK;
+    if (!topk_idxs || !start_pos) return SATTN_ERR_INVALID_ARG;
+    if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(topk_idxs) & 15u)) return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_topk_idxs(topk_idxs, start_pos, B, M, K, win, ratio, *dev, s), s);
+}
+
+sattn_status sattn_kv_ring_write(void *kv_cache, const void *kv_new, const int32_t *start_pos,
+                                 int32_t B, int32_t S, int32_t N, int32_t d, int32_t win,
+                                 sattn_dtype dtype, void *cuda_stream) {
+    if (B < 0 || S < 0 || d <= 0 || win < 1 || N < win || !valid_dtype(dtype))
+        return SATTN_ERR_INVALID_ARG;
+    const int elem = dtype == SATTN_BF16 ? 2 : 4;
+    if ((d * elem) % 16 != 0) return SATTN_ERR_INVALID_ARG;
+    if ((long long)B * S == 0) return SATTN_OK;
+    if (!kv_cache || !kv_new || !start_pos) return SATTN_ERR_INVALID_ARG;
+    if (!aligned16(kv_cache) || !aligned16(kv_new)) return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_kv_ring_write(kv_cache, kv_new, start_pos, B, S, N, d, win, elem, *dev, s),
+                  s);
+}
+
 sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,
                                     const uint8_t *block_mask, int32_t M, int32_t Nctx, int32_t H,
                                     int32_t Hkv, int32_t d, int32_t q_pos0, int32_t kv_begin,

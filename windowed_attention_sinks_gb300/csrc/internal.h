@@ -87,6 +87,11 @@ struct MergeArgs {
 cudaError_t launch_window_simt(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_sparse_simt(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_block_simt(const BlockArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_topk_idxs(int32_t *out, const int32_t *start_pos, int B, int M, int K, int win,
+                             int ratio, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_kv_ring_write(void *cache, const void *src, const int32_t *start_pos, int B,
+                                 int S, int N, int d, int win, int elem_bytes, const DevInfo &dev,
+                                 cudaStream_t s);
 // after_primary: launched as a programmatic dependent of the kernel just
 // issued on `s` (that kernel triggers early; the merge waits for its results).
 cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s,
