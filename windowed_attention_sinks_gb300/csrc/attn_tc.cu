@@ -87,14 +87,27 @@ struct TcParams {
     unsigned *work;  // zeroed per launch: next item to claim
 };
 
+struct Item {
+    bool valid;
+    bool seq_err;
+    int h, g, nq, ntiles;
+    int q_row0;    // first row of the tile in q / o (token index)
+    int key_row0;  // global K/V row of key coordinate 0
+    int qpos0;     // window: local index of query row 0; block: absolute position
+    int lo, hi, L; // window: key band of the tile (local), sequence length
+    const uint8_t *mrow;
+    int kb_lo, kb_hi, kend;  // block: 128-key block range, key limit
+};
+
 struct Bars {
     uint64_t q_full, q_empty, k_full[KSTAGES], k_empty[KSTAGES], v_full[VSTAGES], v_empty[VSTAGES];
     // p_full is per P buffer: a softmax warp may run one tile ahead of the
     // others, so arrivals for consecutive tiles must not share a barrier.
     uint64_t s_full, s_empty, p_full[2], pv_done, o_full, o_empty, drain;
     // items claimed by the producer, handed to the MMA issuer and softmax warps
+    // already decoded (valid = false: no more items)
     uint64_t item_full[ITEM_RING], item_empty[ITEM_RING];
-    int item[ITEM_RING];  // item index, or -1: no more items
+    Item item[ITEM_RING];
 };
 
 // Operand tiles and epilogue staging of one pipeline slot (112 KB).
@@ -120,17 +133,6 @@ struct Smem {
 };
 static_assert(sizeof(Smem) <= 227 * 1024, "shared memory of one CTA");
 
-struct Item {
-    bool valid;
-    bool seq_err;
-    int h, g, nq, ntiles;
-    int q_row0;    // first row of the tile in q / o (token index)
-    int key_row0;  // global K/V row of key coordinate 0
-    int qpos0;     // window: local index of query row 0; block: absolute position
-    int lo, hi, L; // window: key band of the tile (local), sequence length
-    const uint8_t *mrow;
-    int kb_lo, kb_hi, kend;  // block: 128-key block range, key limit
-};
 
 template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &p, int v) {
     Item it;
@@ -265,11 +267,11 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
     // takes the next one) and handed on through the item ring; items past the
     // end of a short sequence are skipped here and never reach the others.
     int ip = 0;  // items published
-    auto publish = [&](int v) -> bool {
+    auto publish = [&](const Item &it) -> bool {
         const int k = ip % ITEM_RING, use = ip / ITEM_RING;
         if (use >= 1 && !mbar_wait(smem_u32(&b.item_empty[k]), (use - 1) & 1, ctx, abort))
             return false;
-        b.item[k] = v;
+        b.item[k] = it;
         mbar_arrive(smem_u32(&b.item_full[k]));
         ++ip;
         return true;
@@ -304,7 +306,7 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
             }
             continue;
         }
-        if (!(ok = publish(v))) break;
+        if (!(ok = publish(it))) break;
         if (it.ntiles == 0) continue;
         if (qi >= 1) ok = mbar_wait(smem_u32(&b.q_empty), (qi - 1) & 1, ctx, abort);
         if (!ok) break;
@@ -324,7 +326,10 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
         if (ok) ok = load_v(it.g, prev_row);
         if (!ok) break;
     }
-    if (ok) ok = publish(-1);
+    if (ok) {
+        Item end{};  // valid = false: no more items
+        ok = publish(end);
+    }
     if (!ok) {
         // Let copies already in flight land before the CTA leaves (bounded).
         int zero = 0;
@@ -354,10 +359,9 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
     for (int ic = 0; ok; ++ic) {
         const int slot_k = ic % ITEM_RING;
         if (!mbar_wait(smem_u32(&b.item_full[slot_k]), (ic / ITEM_RING) & 1, ctx, abort)) break;
-        const int v = b.item[slot_k];
+        const Item it = b.item[slot_k];
         mbar_arrive(smem_u32(&b.item_empty[slot_k]));
-        if (v < 0) break;
-        const Item it = decode_item<MODE>(p, v);
+        if (!it.valid) break;
         if (it.ntiles == 0) continue;
         ok = mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort);
         const int n = it.ntiles, kt0 = kt;
@@ -510,11 +514,10 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
             ok = false;
             break;
         }
-        const int v = b.item[slot_k];
+        const Item it = b.item[slot_k];
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&b.item_empty[slot_k]));
-        if (v < 0) break;
-        const Item it = decode_item<MODE>(p, v);
+        if (!it.valid) break;
         const bool row_valid = r < it.nq;
         if (it.ntiles == 0) {  // block mode: nothing visible in this chunk
             if (MODE == MODE_BLOCK && row_valid) {
