@@ -97,6 +97,7 @@ struct Item {
     int lo, hi, L; // window: key band of the tile (local), sequence length
     const uint8_t *mrow;
     int kb_lo, kb_hi, kend;  // block: 128-key block range, key limit
+    float sink;              // window: the head's sink (0 when there is none)
 };
 
 struct Bars {
@@ -139,6 +140,7 @@ template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &
     it.valid = false;
     it.seq_err = false;
     it.ntiles = 0;
+    it.sink = 0.f;
     it.h = v % p.H;
     it.g = it.h / p.groups;
     const int rest = v / p.H;
@@ -162,6 +164,7 @@ template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &
         it.hi = p.wr < 0 ? it.L - 1 : min(it.L - 1, last + p.wr);
         if (p.causal) it.hi = min(it.hi, last);
         it.ntiles = (it.hi - it.lo + BN) / BN;
+        it.sink = p.sinks ? __ldg(p.sinks + it.h) : 0.f;
         it.valid = true;
     } else {
         const int qb = rest;
@@ -541,7 +544,7 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
         }
         const bool null_sink = MODE == MODE_WINDOW && p.sink_mode == 2;
         const bool key0 = MODE == MODE_WINDOW && p.sink_mode == 1;
-        const float sink = (MODE == MODE_WINDOW && p.sinks) ? __ldg(p.sinks + it.h) : 0.f;
+        const float sink = MODE == MODE_WINDOW ? it.sink : 0.f;
         float m_run = null_sink ? sink * LOG2E : -INFINITY;
         float l = null_sink ? 1.0f : 0.0f;
         const uint64_t scale2 = f2_pack(p.scale_l2, p.scale_l2);
