@@ -71,8 +71,9 @@ def test_static_scratch_matches_workspace_entry_point():
 
 
 def test_static_scratch_refuses_oversized_requests():
-    # 256 single-token requests with long lists, split in two, need about 8.5 MB of partials
-    B, M, H, d, N, K = 256, 1, 32, 128, 16, 4096
+    # 128 single-token requests of 64 heads x 256 with long lists, split in two,
+    # need about 17 MB of partials
+    B, M, H, d, N, K = 128, 1, 64, 256, 16, 4096
     assert sa.sparse_workspace_bytes(B, M, H, d, K) > STATIC_SCRATCH_BYTES
     rng = np.random.default_rng(0)
     case = W.SparseCase(q=W.round_bf16(rng.standard_normal((B, M, H, d)).astype(np.float32)),

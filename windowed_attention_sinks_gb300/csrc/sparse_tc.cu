@@ -53,6 +53,9 @@ constexpr int SLOT_CTRL = GATHER_WARPS + 2;  // control warps of a slot
 // complete, and every reader of ring entry (t+1) % 3 (copies, MMA, softmax of
 // tile t-2) is done by then.
 constexpr int IDX_RING = 3;
+// Index lists stream into shared memory in LCHUNK-entry chunks, NLCH in flight.
+constexpr int LCHUNK = 256;
+constexpr int NLCH = 2;
 constexpr int NTHREADS = 32 * NSLOT * (SLOT_CTRL + 4);
 constexpr int SOFTMAX_THREADS = 128;
 constexpr uint32_t KV_TILE = R * HD * 2;   // 32 KB
@@ -70,6 +73,7 @@ constexpr uint32_t S_COL = 0, O_COL = 64;
 
 struct SlotBars {
     uint64_t idx_ready[IDX_RING];  // lead gather warp -> the other gather warps
+    uint64_t lst_full[NLCH];       // index-list chunk landed
     uint64_t q_full, q_empty;
     uint64_t kv_full[2], kv_empty[2];
     uint64_t s_full[2], s_empty[2];
@@ -83,6 +87,7 @@ struct alignas(1024) SlotSmem {
     uint8_t q[2 * QP_HALF];
     uint8_t p[2][2 * QP_HALF];
     float tbuf[4][NH * TB_STRIDE];
+    int lst[NLCH][LCHUNK];   // index-list chunks, as stored
     // Ring of compacted tiles: tile t uses entry t % IDX_RING
     int idx[IDX_RING][R];    // entries (-1 past the count)
     int tile_cnt[IDX_RING];  // rows that hold entries
@@ -246,6 +251,17 @@ __device__ void gather_helper(const SpParams &p, SlotSmem &sm, volatile int *abo
     __syncwarp();
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory, completion on `bar` (tx bytes).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &sm,
                             volatile int *abort, int first, int stride, const DevCtx &ctx) {
     SlotBars &b = sm.b;
@@ -254,22 +270,46 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
     const int nitems = p.B * p.M * p.splits;
     int qi = 0, gt = 0;  // items started, tiles issued
     bool ok = true, bad = false;
-    // pull an item's slice of the index list into L2 ahead of its use
-    auto prefetch_list = [&](int item) {
-        if (item >= nitems) return;
-        const ItemInfo ni = item_info(p, item);
-        const char *base = reinterpret_cast<const char *>(p.idx + (size_t)ni.bm * p.K + ni.e_begin);
-        const int bytes = (ni.e_end - ni.e_begin) * 4;
-        for (int off = lane * 128; off < bytes; off += 32 * 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
+    // The slot's index lists stream into a ring of NLCH chunks in shared
+    // memory, by bulk copies (rows of the list 16-byte aligned: K % 4 == 0 and
+    // an aligned base) or else by the warp itself. The issue cursor (item,
+    // offset) runs NLCH chunks ahead of compaction.
+    const bool bulk = (p.K & 3) == 0 && (reinterpret_cast<uintptr_t>(p.idx) & 15u) == 0;
+    int is_item = first, is_off = 0, n_iss = 0, n_con = 0;
+    auto issue_chunk = [&]() {
+        while (is_item < nitems) {
+            const ItemInfo ni = item_info(p, is_item);
+            const int e0 = ni.e_begin + is_off;
+            if (e0 >= ni.e_end) {  // next item
+                is_item += stride;
+                is_off = 0;
+                continue;
+            }
+            const int n = min(LCHUNK, ni.e_end - e0);
+            const int slot = n_iss % NLCH;
+            const int32_t *src = p.idx + (size_t)ni.bm * p.K + e0;
+            const uint32_t bar = smem_u32(&b.lst_full[slot]);
+            if (bulk) {
+                if (lane == 0) {
+                    fence_proxy_async_smem();  // earlier reads of the slot come first
+                    mbar_arrive_expect_tx(bar, (uint32_t)n * 4u);
+                    bulk_load(smem_u32(sm.lst[slot]), src, (uint32_t)n * 4u, bar);
+                }
+            } else {
+                for (int i = lane; i < n; i += 32) sm.lst[slot][i] = __ldg(src + i);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar);
+            }
+            is_off += LCHUNK;
+            ++n_iss;
+            return;
+        }
     };
     if (lane == 0) prefetch_tmap(tq);
-    prefetch_list(first);
+    for (int k = 0; k < NLCH; ++k) issue_chunk();
     for (int item = first; ok && item < nitems; item += stride) {
         const ItemInfo it = item_info(p, item);
-        const int32_t *list = p.idx + (size_t)it.bm * p.K;
         const int row0 = it.b * p.N;  // first cache row of this request
-        prefetch_list(item + stride);
         // Q rows of the query (32 heads x 256 B): two 64-column boxes
         if (qi >= 1 && !warp_wait(b.q_empty, (qi - 1) & 1, ctx, abort)) { ok = false; break; }
         if (lane == 0) {
@@ -300,52 +340,49 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
             ring = gt % IDX_RING;
             return true;
         };
-        // Index loads are only issued here (addresses clamped into the slice);
-        // their values are first used, and validated, one group later.
-        auto load = [&](int (&v)[4], int e0) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) v[c] = __ldg(list + min(e0 + 32 * c + lane, it.e_end - 1));
-        };
         int pos = 0;
-        // compact one group of 128 entries (starting at e0) into the open tile
-        auto compact = [&](const int (&v)[4], int e0) {
+        for (int c0 = it.e_begin; ok && c0 < it.e_end; c0 += LCHUNK) {
+            const int slot = n_con % NLCH;
+            if (!warp_wait(b.lst_full[slot], (n_con / NLCH) & 1, ctx, abort)) {
+                ok = false;
+                break;
+            }
+            const int *lst = sm.lst[slot];
+            const int n = min(LCHUNK, it.e_end - c0);
+            // groups of 128 entries: ballot-compact the valid ones into the open tile
+            for (int g0 = 0; ok && g0 < n; g0 += R) {
+                int v[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                int x = v[c];
-                if (e0 + 32 * c + lane >= it.e_end) {
-                    x = -1;
-                } else if (x < -1 || x >= p.N) {
-                    bad = true;
-                    x = -1;
+                for (int c = 0; c < 4; ++c) {
+                    const int i = g0 + 32 * c + lane;
+                    v[c] = i < n ? lst[i] : -1;
                 }
-                const bool valid = x >= 0;
-                const uint32_t bal = __ballot_sync(0xffffffffu, valid);
-                const int cnt = __popc(bal);
-                if (cnt == 0) continue;
-                if (pos + cnt > R) {  // does not fit: issue this tile, open the next
-                    __syncwarp();
-                    if (!close_tile(pos, false)) {
-                        ok = false;
-                        return;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    int x = v[c];
+                    if (x < -1 || x >= p.N) {
+                        bad = true;
+                        x = -1;
                     }
-                    pos = 0;
+                    const bool valid = x >= 0;
+                    const uint32_t bal = __ballot_sync(0xffffffffu, valid);
+                    const int cnt = __popc(bal);
+                    if (cnt == 0) continue;
+                    if (pos + cnt > R) {  // does not fit: issue this tile, open the next
+                        __syncwarp();
+                        if (!close_tile(pos, false)) {
+                            ok = false;
+                            break;
+                        }
+                        pos = 0;
+                    }
+                    if (valid) sm.idx[ring][pos + __popc(bal & lt_mask)] = x;
+                    pos += cnt;
                 }
-                if (valid) sm.idx[ring][pos + __popc(bal & lt_mask)] = x;
-                pos += cnt;
             }
-        };
-        if (it.e_end > it.e_begin) {
-            // two groups of indices in flight: each is loaded one group ahead of use
-            int va[4], vb[4];
-            load(va, it.e_begin);
-            load(vb, it.e_begin + R);
-            for (int e0 = it.e_begin; ok && e0 < it.e_end; e0 += 2 * R) {
-                compact(va, e0);
-                load(va, e0 + 2 * R);
-                if (!ok || e0 + R >= it.e_end) break;
-                compact(vb, e0 + R);
-                load(vb, e0 + 3 * R);
-            }
+            __syncwarp();  // the chunk's reads are done: refill its slot
+            ++n_con;
+            if (ok) issue_chunk();
         }
         if (!ok) break;
         __syncwarp();
@@ -362,9 +399,11 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
     if (bad) record_error(ctx, DEVERR_INDEX);
     // the last Q load lands before the CTA may exit (on the normal path it was
     // consumed already; this matters after an abort)
-    if (lane == 0 && qi >= 1) {
+    if (lane == 0) {
         int zero = 0;
-        mbar_wait(smem_u32(&b.q_full), (qi - 1) & 1, ctx, &zero);
+        if (qi >= 1) mbar_wait(smem_u32(&b.q_full), (qi - 1) & 1, ctx, &zero);
+        for (int k = n_con; k < n_iss; ++k)  // list copies still in flight
+            mbar_wait(smem_u32(&b.lst_full[k % NLCH]), (k / NLCH) & 1, ctx, &zero);
     }
     __syncwarp();
 }
@@ -698,6 +737,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const
                 mbar_init(smem_u32(&b.p_empty[i]), 1);
             }
             for (int i = 0; i < IDX_RING; ++i) mbar_init(smem_u32(&b.idx_ready[i]), 1);
+            for (int i = 0; i < NLCH; ++i) mbar_init(smem_u32(&b.lst_full[i]), 1);
             mbar_init(smem_u32(&b.q_full), 1);
             mbar_init(smem_u32(&b.q_empty), 1);
             mbar_init(smem_u32(&b.pv_done), 1);
