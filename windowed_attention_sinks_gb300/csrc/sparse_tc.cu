@@ -310,15 +310,7 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
     for (int item = first; ok && item < nitems; item += stride) {
         const ItemInfo it = item_info(p, item);
         const int row0 = it.b * p.N;  // first cache row of this request
-        // Q rows of the query (32 heads x 256 B): two 64-column boxes
-        if (qi >= 1 && !warp_wait(b.q_empty, (qi - 1) & 1, ctx, abort)) { ok = false; break; }
-        if (lane == 0) {
-            const uint32_t bar = smem_u32(&b.q_full);
-            mbar_arrive_expect_tx(bar, 2 * QP_HALF);
-            tma_load_2d(smem_u32(sm.q), tq, bar, 0, it.bm * NH);
-            tma_load_2d(smem_u32(sm.q) + QP_HALF, tq, bar, 64, it.bm * NH);
-        }
-        ++qi;
+        bool q_loaded = false;
         int ring = gt % IDX_RING;  // ring entry of the tile being compacted
         // Publish and issue the compacted tile gt holding `pos` rows.
         auto close_tile = [&](int pos, bool last) -> bool {
@@ -332,6 +324,20 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&b.idx_ready[ring]));
+            // Q rows of the query (32 heads x 256 B, two 64-column boxes) once
+            // the previous item's last S was issued; the item's first rows are
+            // already being copied meanwhile
+            if (!q_loaded) {
+                if (qi >= 1 && !warp_wait(b.q_empty, (qi - 1) & 1, ctx, abort)) return false;
+                if (lane == 0) {
+                    const uint32_t bar = smem_u32(&b.q_full);
+                    mbar_arrive_expect_tx(bar, 2 * QP_HALF);
+                    tma_load_2d(smem_u32(sm.q), tq, bar, 0, it.bm * NH);
+                    tma_load_2d(smem_u32(sm.q) + QP_HALF, tq, bar, 64, it.bm * NH);
+                }
+                ++qi;
+                q_loaded = true;
+            }
             // kv_full of this stage may take this arrival only once the stage's
             // previous tile is consumed (which also keeps the ring safe)
             if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) return false;
