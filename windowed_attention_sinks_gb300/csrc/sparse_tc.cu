@@ -48,11 +48,10 @@ constexpr int NSLOT = 2;         // independent item streams per CTA
 // warp's copies would stall its compaction), one warp issues the MMAs.
 constexpr int GATHER_WARPS = 4;
 constexpr int SLOT_CTRL = GATHER_WARPS + 2;  // control warps of a slot
-// Compacted-index ring depth. The lead gather warp compacts tile t+1 only
-// after acquiring the KV stage of tile t, i.e. after P V of tile t-2 is
-// complete, and every reader of ring entry (t+1) % 3 (copies, MMA, softmax of
-// tile t-2) is done by then.
-constexpr int IDX_RING = 3;
+// Compacted-index ring depth: the lead warp runs up to IDX_RING - 1 tiles
+// ahead of the slowest reader of the ring (copy warps, MMA, softmax warps),
+// each of which releases an entry (idx_empty) once it has read it.
+constexpr int IDX_RING = 5;
 // Index lists stream into shared memory in LCHUNK-entry chunks, NLCH in flight.
 constexpr int LCHUNK = 256;
 constexpr int NLCH = 2;
@@ -72,7 +71,8 @@ constexpr uint32_t TMEM_COLS = SLOT_COLS * NSLOT;
 constexpr uint32_t S_COL = 0, O_COL = 64;
 
 struct SlotBars {
-    uint64_t idx_ready[IDX_RING];  // lead gather warp -> the other gather warps
+    uint64_t idx_ready[IDX_RING];  // lead gather warp -> copy warps, MMA, softmax
+    uint64_t idx_empty[IDX_RING];  // readers -> lead gather warp
     uint64_t lst_full[NLCH];       // index-list chunk landed
     uint64_t q_full, q_empty;
     uint64_t kv_full[2], kv_empty[2];
@@ -190,9 +190,9 @@ __device__ __forceinline__ ItemInfo item_info(const SpParams &p, int item) {
 
 // Copy warp g of a slot copies rows 2i + hi, i in [PAIRS g, PAIRS (g+1)), of
 // each tile. The lead warp loads Q, compacts the index lists into the ring
-// and publishes each ring entry to the copy warps (idx_ready) and, once the
-// tile's stage is free, to the MMA and softmax roles (kv_full); after the
-// last tile it publishes an entry with tile_row0 = -1.
+// and publishes each ring entry to the copy warps, the MMA and the softmax
+// warps (idx_ready); after the last tile it publishes an entry with
+// tile_row0 = -1.
 constexpr int PAIRS = R / 2 / GATHER_WARPS;  // row pairs per warp (multiple of 4)
 
 struct RowCopier {
@@ -246,6 +246,8 @@ __device__ void gather_helper(const SpParams &p, SlotSmem &sm, volatile int *abo
         if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) break;
         cp.issue(smem_u32(sm.kv[st]), sm.idx[r], p.kv + (size_t)row0 * HD, g);
         cp_async_arrive(smem_u32(&b.kv_full[st]));
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&b.idx_empty[r]));
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
@@ -314,7 +316,6 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
         int ring = gt % IDX_RING;  // ring entry of the tile being compacted
         // Publish and issue the compacted tile gt holding `pos` rows.
         auto close_tile = [&](int pos, bool last) -> bool {
-            const int st = gt & 1, use = gt >> 1;
             int *ids = sm.idx[ring];
             for (int r = pos + lane; r < R; r += 32) ids[r] = -1;
             if (lane == 0) {
@@ -338,13 +339,11 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
                 ++qi;
                 q_loaded = true;
             }
-            // kv_full of this stage may take this arrival only once the stage's
-            // previous tile is consumed (which also keeps the ring safe)
-            if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) return false;
-            if (lane == 0) mbar_arrive(smem_u32(&b.kv_full[st]));  // ring entry -> MMA, softmax
             ++gt;
             ring = gt % IDX_RING;
-            return true;
+            // the next entry is written once its previous tile's readers let go
+            return gt < IDX_RING ||
+                   warp_wait(b.idx_empty[ring], ((gt / IDX_RING) - 1) & 1, ctx, abort);
         };
         int pos = 0;
         for (int c0 = it.e_begin; ok && c0 < it.e_end; c0 += LCHUNK) {
@@ -395,7 +394,7 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
         // an item without valid entries still gets one (empty) tile
         if (!close_tile(pos, true)) { ok = false; break; }
     }
-    if (ok) {  // no more tiles (the ring entry is free: see IDX_RING)
+    if (ok) {  // no more tiles (the next ring entry was opened by the last close_tile)
         const int ring = gt % IDX_RING;
         if (lane == 0) {
             sm.tile_row0[ring] = -1;
@@ -449,9 +448,11 @@ __device__ void mma_role(const SpParams &p, SlotSmem &sm, volatile int *abort, u
             const int st = s_t & 1, use = s_t >> 1;
             if ((!s_first || mbar_try_wait(smem_u32(&b.q_full), s_item & 1)) &&
                 (use == 0 || mbar_try_wait(smem_u32(&b.s_empty[st]), (use - 1) & 1)) &&
-                mbar_try_wait(smem_u32(&b.kv_full[st]), use & 1)) {
+                mbar_try_wait(smem_u32(&b.kv_full[st]), use & 1) &&
+                mbar_try_wait(smem_u32(&b.idx_ready[s_t % IDX_RING]), (s_t / IDX_RING) & 1)) {
                 tc_fence_after();
                 const bool last = sm.tile_last[s_t % IDX_RING] != 0;
+                mbar_arrive(smem_u32(&b.idx_empty[s_t % IDX_RING]));
                 const uint64_t a = st ? dkv1 : dkv0;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
@@ -553,11 +554,11 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
         int j = 0;
         for (bool last = false; !last; ++j) {
             const int t = gt0 + j, st = t & 1, use = t >> 1, ring = t % IDX_RING;
-            // S^T of this tile; its ring entry was published with kv_full; P
-            // buffer st was last read by P V of tile t-2
+            // the tile's ring entry, S^T of the tile; P buffer st was last read
+            // by P V of tile t-2
             if (!failed) {
-                failed = !mbar_wait(smem_u32(&b.s_full[st]), use & 1, ctx, abort) ||
-                         !mbar_wait(smem_u32(&b.kv_full[st]), use & 1, ctx, abort) ||
+                failed = !mbar_wait(smem_u32(&b.idx_ready[ring]), (t / IDX_RING) & 1, ctx, abort) ||
+                         !mbar_wait(smem_u32(&b.s_full[st]), use & 1, ctx, abort) ||
                          (use >= 1 &&
                           !mbar_wait(smem_u32(&b.p_empty[st]), (use - 1) & 1, ctx, abort));
             }
@@ -584,6 +585,7 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
                     x[4 * k + 2] = f.z;
                     x[4 * k + 3] = f.w;
                 }
+                // the ring entry is read here, then released to the lead warp
                 last = sm.tile_last[ring] != 0;
                 if (key0) {  // the sink bias on the logit of key 0, in raw-score units
                     const int *ids = &sm.idx[ring][quarter * 32];
@@ -597,6 +599,8 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
                     }
                 }
                 const int nvalid = sm.tile_cnt[ring] - quarter * 32;  // keys of this warp holding entries
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&b.idx_empty[ring]));
                 if (nvalid < 32) {
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
@@ -735,14 +739,17 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const
         for (int s = 0; s < NSLOT; ++s) {
             SlotBars &b = all.slot[s].b;
             for (int i = 0; i < 2; ++i) {
-                mbar_init(smem_u32(&b.kv_full[i]), 32 * GATHER_WARPS + 1);  // copies + publish
+                mbar_init(smem_u32(&b.kv_full[i]), 32 * GATHER_WARPS);  // every copying lane
                 mbar_init(smem_u32(&b.kv_empty[i]), 1);
                 mbar_init(smem_u32(&b.s_full[i]), 1);
                 mbar_init(smem_u32(&b.s_empty[i]), 4);
                 mbar_init(smem_u32(&b.p_full[i]), 4);
                 mbar_init(smem_u32(&b.p_empty[i]), 1);
             }
-            for (int i = 0; i < IDX_RING; ++i) mbar_init(smem_u32(&b.idx_ready[i]), 1);
+            for (int i = 0; i < IDX_RING; ++i) {
+                mbar_init(smem_u32(&b.idx_ready[i]), 1);
+                mbar_init(smem_u32(&b.idx_empty[i]), GATHER_WARPS + 1 + 4);  // copy, MMA, softmax
+            }
             for (int i = 0; i < NLCH; ++i) mbar_init(smem_u32(&b.lst_full[i]), 1);
             mbar_init(smem_u32(&b.q_full), 1);
             mbar_init(smem_u32(&b.q_empty), 1);
