@@ -309,10 +309,39 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
     };
     if (lane == 0) prefetch_tmap(tq);
     for (int k = 0; k < NLCH; ++k) issue_chunk();
+    // Q rows of a query (32 heads x 256 B, two 64-column boxes) go to the
+    // slot's Q buffer once the previous item's last S was issued. The lead
+    // polls for that between tiles and blocks only when it is a whole item
+    // ahead (or at the end).
+    int q_pend = -1;  // query row (b, m) whose Q copy is still to be issued
+    auto issue_q = [&](bool block) -> bool {
+        if (q_pend < 0) return true;
+        if (qi >= 1) {
+            if (block) {
+                if (!warp_wait(b.q_empty, (qi - 1) & 1, ctx, abort)) return false;
+            } else {
+                int r = lane == 0 ? (mbar_try_wait(smem_u32(&b.q_empty), (qi - 1) & 1) ? 1 : 0) : 0;
+                if (!__shfl_sync(0xffffffffu, r, 0)) return true;  // not yet
+            }
+        }
+        if (lane == 0) {
+            const uint32_t bar = smem_u32(&b.q_full);
+            mbar_arrive_expect_tx(bar, 2 * QP_HALF);
+            tma_load_2d(smem_u32(sm.q), tq, bar, 0, q_pend * NH);
+            tma_load_2d(smem_u32(sm.q) + QP_HALF, tq, bar, 64, q_pend * NH);
+        }
+        ++qi;
+        q_pend = -1;
+        return true;
+    };
     for (int item = first; ok && item < nitems; item += stride) {
         const ItemInfo it = item_info(p, item);
         const int row0 = it.b * p.N;  // first cache row of this request
-        bool q_loaded = false;
+        if (!issue_q(true)) {  // the previous item's Q first
+            ok = false;
+            break;
+        }
+        q_pend = it.bm;
         int ring = gt % IDX_RING;  // ring entry of the tile being compacted
         // Publish and issue the compacted tile gt holding `pos` rows.
         auto close_tile = [&](int pos, bool last) -> bool {
@@ -325,25 +354,18 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&b.idx_ready[ring]));
-            // Q rows of the query (32 heads x 256 B, two 64-column boxes) once
-            // the previous item's last S was issued; the item's first rows are
-            // already being copied meanwhile
-            if (!q_loaded) {
-                if (qi >= 1 && !warp_wait(b.q_empty, (qi - 1) & 1, ctx, abort)) return false;
-                if (lane == 0) {
-                    const uint32_t bar = smem_u32(&b.q_full);
-                    mbar_arrive_expect_tx(bar, 2 * QP_HALF);
-                    tma_load_2d(smem_u32(sm.q), tq, bar, 0, it.bm * NH);
-                    tma_load_2d(smem_u32(sm.q) + QP_HALF, tq, bar, 64, it.bm * NH);
-                }
-                ++qi;
-                q_loaded = true;
-            }
+            issue_q(false);
             ++gt;
             ring = gt % IDX_RING;
-            // the next entry is written once its previous tile's readers let go
-            return gt < IDX_RING ||
-                   warp_wait(b.idx_empty[ring], ((gt / IDX_RING) - 1) & 1, ctx, abort);
+            // the next entry is written once its previous tile's readers let
+            // go. Before blocking on that, the pending Q is issued: S of the
+            // entry's previous tile may need it (the Q wait itself only needs
+            // the previous item's tiles, all published).
+            if (gt < IDX_RING) return true;
+            const int par = ((gt / IDX_RING) - 1) & 1;
+            int r = lane == 0 ? (mbar_try_wait(smem_u32(&b.idx_empty[ring]), par) ? 1 : 0) : 0;
+            if (__shfl_sync(0xffffffffu, r, 0)) return true;
+            return issue_q(true) && warp_wait(b.idx_empty[ring], par, ctx, abort);
         };
         int pos = 0;
         for (int c0 = it.e_begin; ok && c0 < it.e_end; c0 += LCHUNK) {
@@ -354,13 +376,20 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
             }
             const int *lst = sm.lst[slot];
             const int n = min(LCHUNK, it.e_end - c0);
-            // groups of 128 entries: ballot-compact the valid ones into the open tile
+            // groups of 128 entries (four consecutive ones per lane): ballot-
+            // compact the valid ones into the open tile
             for (int g0 = 0; ok && g0 < n; g0 += R) {
                 int v[4];
+                const int i0 = g0 + 4 * lane;
+                if (i0 + 4 <= n) {
+                    const int4 q4 = *reinterpret_cast<const int4 *>(lst + i0);
+                    v[0] = q4.x;
+                    v[1] = q4.y;
+                    v[2] = q4.z;
+                    v[3] = q4.w;
+                } else {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int i = g0 + 32 * c + lane;
-                    v[c] = i < n ? lst[i] : -1;
+                    for (int c = 0; c < 4; ++c) v[c] = i0 + c < n ? lst[i0 + c] : -1;
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
@@ -387,13 +416,17 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
             }
             __syncwarp();  // the chunk's reads are done: refill its slot
             ++n_con;
-            if (ok) issue_chunk();
+            if (ok) {
+                issue_chunk();
+                issue_q(false);
+            }
         }
         if (!ok) break;
         __syncwarp();
         // an item without valid entries still gets one (empty) tile
         if (!close_tile(pos, true)) { ok = false; break; }
     }
+    if (ok && !issue_q(true)) ok = false;  // the last item's Q
     if (ok) {  // no more tiles (the next ring entry was opened by the last close_tile)
         const int ring = gt % IDX_RING;
         if (lane == 0) {
