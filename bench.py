@@ -461,7 +461,11 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                    else "inputs larger than L2",
                    "launch": "CUDA graph replay" if graph is not None else "direct"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                     "frac": gbs / peak, "traffic": None, "peak_source": peaks_src,
+                     "frac": gbs / peak,
+                     "traffic": profiled_traffic("sparse_tc_kernel<%s>" % args.workload,
+                                                 "sparse_tc.cu", units)
+                     if args.workload in ("decode", "prefill") else None,
+                     "peak_source": peaks_src,
                      "tflops": tf,
                      "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
         # sparse: the gathered-attention kernel, plus the merge when lists are split
