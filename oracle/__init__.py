@@ -5,10 +5,12 @@ benchmark's CPU-baseline leg are the only callers. The library path never
 imports this package. The C source (`sattn_oracle.c`) shares nothing with the
 CUDA implementation.
 
-The attention functions take float32 numpy arrays (the exact input values,
-bf16 inputs widened) and return float64 outputs; `topk_idxs` and
-`kv_ring_write` (cache bookkeeping around the path) are plain Python. Each accepts an optional `rows` array of
-row ids so that large workloads can be checked on sampled rows:
+`topk_idxs` and `kv_ring_write` (cache bookkeeping around the path) are
+plain Python, and `compress_kv` (the compressor's gated pooling) is numpy
+fp64. The attention functions take float32 numpy arrays (the exact input
+values, bf16 inputs widened) and return float64 outputs; each accepts an
+optional `rows` array of row ids so that large workloads can be checked on
+sampled rows:
   window:  row = token * H + head
   sparse:  row = (b * M + m) * H + head
   block:   row = i * H + head
@@ -211,3 +213,52 @@ def kv_ring_write(kv_cache, kv_new, start_pos, win):
         out[b, cutoff:cutoff + first] = block[:first]
         out[b, :n - first] = block[first:]
     return out
+
+
+# ---------------------------------------------------------------------------
+# Compressor gated pooling ("DeepSeek-V4 CSA/HCA walkthrough", sections 5.1
+# and 5.2). numpy fp64, steps in the pages' order.
+
+def compress_kv(kv, score, ape, ratio, overlap):
+    """Gated pooling of every `ratio` consecutive tokens into one compressed
+    row; returns float64 [B, S // ratio, d].
+
+    kv, score: [B, S, coff * d] with coff = 2 when `overlap` else 1 (the
+    token projections the pages call wkv(x) and wgate(x)); ape: [ratio,
+    coff * d], the learned absolute position term. The S % ratio tail tokens
+    produce no row (the pages keep them in kv_state / score_state until their
+    window is complete).
+
+      1. the first S - S % ratio tokens form windows of `ratio` tokens;
+      2. ape is added to each window's scores (entry i gets ape[i]);
+      3. with overlap each window [ratio, 2d] becomes [2 ratio, d]: entries
+         ratio .. 2 ratio - 1 are its own tokens' last d columns, entries
+         0 .. ratio - 1 the previous window's tokens' first d columns; window 0
+         has no previous window, so those entries hold kv = 0 and score = -inf
+         (weight 0 after the softmax);
+      4. softmax of the scores over the window entries, for each column;
+      5. the row is the sum over the entries of kv times those weights.
+    """
+    kv = np.asarray(kv, dtype=np.float64)
+    score = np.asarray(score, dtype=np.float64)
+    ape = np.asarray(ape, dtype=np.float64)
+    B, S, W = kv.shape
+    coff = 2 if overlap else 1
+    d = W // coff
+    n = S // ratio
+    kv_w = kv[:, :n * ratio].reshape(B, n, ratio, W)
+    sc_w = score[:, :n * ratio].reshape(B, n, ratio, W) + ape
+    if overlap:
+        kv_o = np.zeros((B, n, 2 * ratio, d))
+        sc_o = np.full((B, n, 2 * ratio, d), -np.inf)
+        kv_o[:, :, ratio:] = kv_w[..., d:]
+        sc_o[:, :, ratio:] = sc_w[..., d:]
+        kv_o[:, 1:, :ratio] = kv_w[:, :-1, :, :d]
+        sc_o[:, 1:, :ratio] = sc_w[:, :-1, :, :d]
+        kv_w, sc_w = kv_o, sc_o
+    if n == 0:
+        return np.zeros((B, 0, d))
+    m = sc_w.max(axis=2, keepdims=True)
+    e = np.exp(sc_w - m)
+    weights = e / e.sum(axis=2, keepdims=True)
+    return (kv_w * weights).sum(axis=2)
