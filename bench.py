@@ -8,8 +8,10 @@ and both sink semantics (key-0 bias and null logit), four launches of
 sattn_window_fwd over device-resident inputs. The metric is queries/s (query
 tokens per second, all four passes counted).
 
-Other workloads (--workload decode | prefill | block) measure the gathered
-decode / prefill and the chunked block-sparse paths the same way.
+Other workloads (--workload decode | prefill | block | index | compress)
+measure the gathered decode / prefill path, the chunked block-sparse path,
+the cache bookkeeping (index lists + ring write) and the compressor's gated
+pooling the same way.
 
 Output: one JSON line on rank 0. Timing: W warm-up steps, then K steps between
 a barrier + device synchronisation on both sides, CUDA events on the launch
@@ -388,6 +390,32 @@ def run_other(args, rank, world, device, peaks, peaks_src):
             sa.build_topk_idxs(starts, M, K, win, ratio, out=idx_out, stream=st or stream)
             sa.kv_ring_write(cache, new_kv, starts, win, stream=st or stream)
         name = "cache bookkeeping: topk index lists (8192 queries, K=2048, win 128, ratio 4) + ring write"
+    elif args.workload == "compress":
+        # compressor gated pooling: eight 32K-token prefills at ratio 4 with
+        # overlapping windows, fp32 projections in, bf16 rows into the
+        # compressed region of each request's cache
+        nb = 0
+        case = W.compress_case(seed)
+        B, S, Wd = case.kv.shape
+        d, ratio, win = case.d, case.ratio, 128
+        nwin = S // ratio
+        kvp = torch.from_numpy(case.kv).to(device)
+        scp = torch.from_numpy(case.score).to(device)
+        ape = torch.from_numpy(case.ape).to(device)
+        cache = torch.zeros((B, win + nwin, d), dtype=bf, device=device)
+        rows = cache[:, win:]
+        # every projection element read once (the last window's first half is
+        # never needed), each row written once
+        nbytes = (B * (nwin * ratio * d * (2 if case.overlap else 1)
+                       - (ratio * d if case.overlap else 0)) * 2 * 4 + B * nwin * d * 2)
+        flops = 0
+        units = B * nwin
+        flush = None
+
+        def launch(st=None):
+            sa.compress_kv(kvp, scp, ape, ratio, case.overlap, out=rows, stream=st or stream)
+        name = "compressor gated pooling: B=%d S=%d d=%d ratio=%d overlap, fp32 in, bf16 rows" % (
+            B, S, d, ratio)
     else:
         nb = 0
         case = W.block_sparse_bf16(seed)
@@ -451,11 +479,15 @@ def run_other(args, rank, world, device, peaks, peaks_src):
     gbs = nbytes / (ms / 1e3) / 1e9
     tf = flops / (ms / 1e3) / 1e12
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    unit_name = "compressed rows" if args.workload == "compress" else "queries"
     return {
-        "metric": "queries/s (%s)" % args.workload, "value": whole_job_rate(units, world, ms),
-        "unit": "queries/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": "%s/s (%s)" % (unit_name, args.workload),
+        "value": whole_job_rate(units, world, ms),
+        "unit": "%s/s" % unit_name, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded numpy PCG64, bf16)",
+        "dtype": "f32" if args.workload == "compress" else "bf16",
+        "data": "synthetic (seeded numpy PCG64%s)" % (
+            ", fp32 projections" if args.workload == "compress" else ", bf16"),
         "config": {"workload": name,
                    "l2": "scratch > L2 rewritten before each step" if flush is not None
                    else "inputs larger than L2",
@@ -569,7 +601,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="sattn", choices=["sattn", "reference"])
     ap.add_argument("--workload", default="window", choices=["window", "decode", "prefill",
-                                                              "block", "index"])
+                                                              "block", "index", "compress"])
     ap.add_argument("--seqs", type=int, default=256,
                     help="window workload: number of sequences (256 = the full workload)")
     ap.add_argument("--no-e2e", action="store_true")

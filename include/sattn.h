@@ -230,6 +230,35 @@ sattn_status sattn_kv_ring_write(void *kv_cache, const void *kv_new, const int32
                                  int32_t B, int32_t S, int32_t N, int32_t d, int32_t win,
                                  sattn_dtype dtype, void *cuda_stream);
 
+/*
+ * Compressor gated pooling (DeepSeek-V4 CSA/HCA walkthrough, sections 5.1 and
+ * 5.2): every `ratio` consecutive tokens of a sequence become one compressed
+ * KV row, the softmax-weighted sum of their kv projections.
+ *
+ *   kv, score [B, S, coff * d] (in_dtype, device, row-major): the tokens' kv
+ *   and gate projections, coff = 2 when `overlap` is 1, else 1.
+ *   ape float32 [ratio, coff * d] (device): the absolute position term.
+ *   out (out_dtype, device, written): row w of sequence b, w = 0 .. S/ratio - 1,
+ *   at out + b * out_batch_stride + w * d elements; e.g. the compressed region
+ *   of a [window | compressed] cache with out_batch_stride = N * d.
+ * For window w and column j (0 <= j < d) the entries are the window's tokens
+ *   t = w * ratio + i, i < ratio, with value kv[t, c] and score score[t, c] +
+ *   ape[i, c] where c = (coff - 1) * d + j; with overlap also the previous
+ *   window's tokens t' = (w - 1) * ratio + i with kv[t', j] and score[t', j] +
+ *   ape[i, j] (window 0 has no previous window). out[w, j] = sum over the
+ *   entries of value * softmax(scores). The S % ratio tail tokens produce no
+ *   row: a decode step passes the tokens of the current and previous window.
+ * Computed in fp32; out rounded to nearest even for BF16.
+ * Requirements: B, S >= 0; ratio >= 1; overlap 0 or 1; d a multiple of 4;
+ *   out_batch_stride >= (S / ratio) * d and a multiple of 4; kv, score, ape and
+ *   out 16-byte aligned; otherwise SATTN_ERR_INVALID_ARG before anything runs.
+ *   The caller owns every buffer; nothing is allocated.
+ */
+sattn_status sattn_compress_kv(const void *kv, const void *score, const float *ape, void *out,
+                               int64_t out_batch_stride, int32_t B, int32_t S, int32_t d,
+                               int32_t ratio, int32_t overlap, sattn_dtype in_dtype,
+                               sattn_dtype out_dtype, void *cuda_stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *sattn_status_str(sattn_status s);
 

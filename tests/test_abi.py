@@ -104,6 +104,21 @@ def test_invalid_arguments_rejected_on_host(lib):
                                    1, None) == 1
     rc = lib.sattn_merge_lse(fake, fake, 2, 10, 0, 8, None, fake, None, 0, None)
     assert rc == 1
+    # compressor: d not a multiple of 4, ratio 0, bad overlap flag, out stride
+    # too small, misaligned pointer; fewer tokens than a window is no work
+    i64 = ctypes.c_int64
+    assert lib.sattn_compress_kv(fake, fake, fake, fake, i64(1000), 2, 64, 6, 4, 1, 0, 0,
+                                 None) == 1
+    assert lib.sattn_compress_kv(fake, fake, fake, fake, i64(1000), 2, 64, 8, 0, 1, 0, 0,
+                                 None) == 1
+    assert lib.sattn_compress_kv(fake, fake, fake, fake, i64(1000), 2, 64, 8, 4, 2, 0, 0,
+                                 None) == 1
+    assert lib.sattn_compress_kv(fake, fake, fake, fake, i64(124), 2, 64, 8, 4, 1, 0, 0,
+                                 None) == 1
+    assert lib.sattn_compress_kv(fake, ctypes.c_void_p(fake.value + 8), fake, fake, i64(128), 2,
+                                 64, 8, 4, 1, 0, 0, None) == 1
+    assert lib.sattn_compress_kv(None, None, None, None, i64(0), 2, 3, 8, 4, 1, 0, 0,
+                                 None) == 0
 
 
 def test_workspace_size_monotone(lib):

@@ -60,6 +60,9 @@ def lib() -> ctypes.CDLL:
     L.sattn_build_topk_idxs.restype = ctypes.c_int
     L.sattn_kv_ring_write.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_int, P]
     L.sattn_kv_ring_write.restype = ctypes.c_int
+    L.sattn_compress_kv.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, ctypes.c_int,
+                                    ctypes.c_int, P]
+    L.sattn_compress_kv.restype = ctypes.c_int
     L.sattn_status_str.argtypes = [ctypes.c_int]
     L.sattn_status_str.restype = ctypes.c_char_p
     L.sattn_set_debug.argtypes = [ctypes.c_int]
@@ -236,6 +239,38 @@ def kv_ring_write(kv_cache, kv_new, start_pos, win, stream=None):
            lib().sattn_kv_ring_write(_ptr(kv_cache), _ptr(kv_new), _ptr(start_pos), B, S, N, d,
                                      int(win), _dtype_code(kv_cache), _stream(stream)))
     return kv_cache
+
+
+def compress_kv(kv, score, ape, ratio, overlap, out=None, out_dtype=None, stream=None):
+    """Compressor gated pooling (sattn_compress_kv): every `ratio` tokens of
+    kv / score [B, S, coff*d] (coff = 2 with overlap) become one row of out
+    [B, S // ratio, d]. `out` may be a view with a batch stride (e.g. the
+    compressed rows of a cache: kv_cache[:, win:win + S // ratio]) whose rows
+    are contiguous; by default a new tensor of `out_dtype` (kv's dtype)."""
+    import torch
+
+    B, S, W = kv.shape
+    coff = 2 if overlap else 1
+    if W % coff:
+        raise ValueError("kv width %d is not a multiple of %d" % (W, coff))
+    d = W // coff
+    _need(kv, "kv", None, kv.device)
+    _need(score, "score", kv.dtype, kv.device)
+    _need(ape, "ape", torch.float32, kv.device)
+    if tuple(score.shape) != tuple(kv.shape) or tuple(ape.shape) != (int(ratio), W):
+        raise ValueError("score must match kv and ape must be [ratio, coff*d]")
+    nwin = S // int(ratio)
+    if out is None:
+        out = torch.empty((B, nwin, d), dtype=out_dtype or kv.dtype, device=kv.device)
+    if out.dim() != 3 or tuple(out.shape) != (B, nwin, d) or out.stride(2) != 1 or \
+            (nwin > 1 and out.stride(1) != d) or out.device != kv.device:
+        raise ValueError("out must be [B, S // ratio, d] with contiguous rows")
+    _check("sattn_compress_kv",
+           lib().sattn_compress_kv(_ptr(kv), _ptr(score), _ptr(ape), _ptr(out),
+                                   int(out.stride(0)) if B > 1 else nwin * d, B, S, d,
+                                   int(ratio), 1 if overlap else 0, _dtype_code(kv),
+                                   _dtype_code(out), _stream(stream)))
+    return out
 
 
 def check_device(stream=None):

@@ -152,7 +152,7 @@ sattn_status check_arch(const DevInfo *dev) {
 
 extern "C" {
 
-int32_t sattn_version(void) { return 100; }
+int32_t sattn_version(void) { return 101; }
 
 const char *sattn_status_str(sattn_status s) {
     switch (s) {
@@ -305,6 +305,29 @@ sattn_status sattn_kv_ring_write(void *kv_cache, const void *kv_new, const int32
     cudaStream_t s = as_stream(cuda_stream);
     return finish(launch_kv_ring_write(kv_cache, kv_new, start_pos, B, S, N, d, win, elem, *dev, s),
                   s);
+}
+
+sattn_status sattn_compress_kv(const void *kv, const void *score, const float *ape, void *out,
+                               int64_t out_batch_stride, int32_t B, int32_t S, int32_t d,
+                               int32_t ratio, int32_t overlap, sattn_dtype in_dtype,
+                               sattn_dtype out_dtype, void *cuda_stream) {
+    if (B < 0 || S < 0 || ratio < 1 || (overlap != 0 && overlap != 1)) return SATTN_ERR_INVALID_ARG;
+    if (d <= 0 || d % 4 != 0 || !valid_dtype(in_dtype) || !valid_dtype(out_dtype))
+        return SATTN_ERR_INVALID_ARG;
+    const int64_t nwin = S / ratio;
+    if (out_batch_stride < nwin * d || out_batch_stride % 4 != 0) return SATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * nwin == 0) return SATTN_OK;
+    if (!kv || !score || !ape || !out) return SATTN_ERR_INVALID_ARG;
+    if (!aligned16(kv) || !aligned16(score) || !aligned16(ape) || !aligned16(out))
+        return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    CompressArgs a{kv, score, ape, out, out_batch_stride, B, S, d, ratio, overlap,
+                   (int)in_dtype, (int)out_dtype};
+    return finish(launch_compress_kv(a, *dev, s), s);
 }
 
 sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,

@@ -83,6 +83,17 @@ struct MergeArgs {
     int dtype;
 };
 
+// Compressor gated pooling: kv / score [B, S, coff*d] (in_dtype), ape fp32
+// [ratio, coff*d], rows to out + b * out_batch_stride + w * d (out_dtype).
+struct CompressArgs {
+    const void *kv, *score;
+    const float *ape;
+    void *out;
+    int64_t out_batch_stride;
+    int B, S, d, ratio, overlap;
+    int in_dtype, out_dtype;
+};
+
 // SIMT kernels: any dtype, d in {64, 128}.
 cudaError_t launch_window_simt(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_sparse_simt(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
@@ -92,6 +103,7 @@ cudaError_t launch_topk_idxs(int32_t *out, const int32_t *start_pos, int B, int 
 cudaError_t launch_kv_ring_write(void *cache, const void *src, const int32_t *start_pos, int B,
                                  int S, int N, int d, int win, int elem_bytes, const DevInfo &dev,
                                  cudaStream_t s);
+cudaError_t launch_compress_kv(const CompressArgs &a, const DevInfo &dev, cudaStream_t s);
 // after_primary: launched as a programmatic dependent of the kernel just
 // issued on `s` (that kernel triggers early; the merge waits for its results).
 cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s,

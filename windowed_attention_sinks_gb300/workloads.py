@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the five attention workloads.
+"""Seeded synthetic inputs for the attention workloads and the compressor.
 
 This module only draws random numbers and builds index structures. It holds
 none of the attention arithmetic, so both the CUDA path and the CPU oracle
@@ -22,6 +22,9 @@ Workload shapes follow the pages:
   * chunked block-sparse: nano-vllm "XAttention Offload Stream
     Synchronization Fix", technical details (4096-key chunks, partial
     (m, l) stats merged afterwards) and test results (~10% density at 32K).
+  * compressor gated pooling: DeepSeek-V4 CSA/HCA walkthrough, sections 2.2
+    (compress_ratio 4) and 5.1-5.2 (kv / gate projections of every token,
+    ape, overlap windows); the projections are drawn directly (no weights).
 """
 from __future__ import annotations
 
@@ -35,7 +38,8 @@ SINK_KEY0_BIAS = 1
 SINK_NULL_LOGIT = 2
 SINK_MODES = {"none": SINK_NONE, "key0_bias": SINK_KEY0_BIAS, "null_logit": SINK_NULL_LOGIT}
 
-_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "kv": 4, "sinks": 5, "lens": 6, "idx": 7, "drop": 8, "mask": 9}
+_TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "kv": 4, "sinks": 5, "lens": 6, "idx": 7, "drop": 8, "mask": 9,
+               "score": 10, "ape": 11}
 
 
 def _rng(workload: int, tensor: str, seed: int) -> np.random.Generator:
@@ -301,3 +305,33 @@ def block_sparse_bf16(seed: int, Nctx: int = 32768, M: int = 4096, H: int = 32, 
         k=round_bf16(_normal(W, "k", seed, (Nctx, Hkv, d))),
         v=round_bf16(_normal(W, "v", seed, (Nctx, Hkv, d))),
         mask=mask, q_pos0=q_pos0, chunk=chunk, scale=1.0 / math.sqrt(d), blk=blk)
+
+
+@dataclass
+class CompressCase:
+    """Compressor inputs: kv / score [B, S, coff*d], ape [ratio, coff*d]."""
+
+    kv: np.ndarray
+    score: np.ndarray
+    ape: np.ndarray
+    ratio: int
+    overlap: bool
+
+    @property
+    def d(self):
+        return self.kv.shape[2] // (2 if self.overlap else 1)
+
+
+def compress_case(seed: int, B: int = 8, S: int = 32768, d: int = 128, ratio: int = 4,
+                  overlap: bool = True, bf16: bool = False) -> CompressCase:
+    """Token projections of B sequences of S tokens for the compressor; the
+    default is the prefill of eight 32K sequences at ratio 4 with overlapping
+    windows (8192 compressed rows each, as in the gathered prefill cache).
+    kv ~ N(0,1), score ~ 2 N(0,1) and ape ~ 0.5 N(0,1), fp32 (or bf16-rounded)."""
+    W = 6
+    coff = 2 if overlap else 1
+    rnd = round_bf16 if bf16 else (lambda x: x)
+    return CompressCase(kv=rnd(_normal(W, "kv", seed, (B, S, coff * d))),
+                        score=rnd(_normal(W, "score", seed, (B, S, coff * d), std=2.0)),
+                        ape=_normal(W, "ape", seed, (ratio, coff * d), std=0.5),
+                        ratio=ratio, overlap=overlap)
