@@ -262,3 +262,78 @@ def compress_kv(kv, score, ape, ratio, overlap):
     e = np.exp(sc_w - m)
     weights = e / e.sum(axis=2, keepdims=True)
     return (kv_w * weights).sum(axis=2)
+
+
+# ---------------------------------------------------------------------------
+# FP8 KV cache ("DeepSeek-V4 CSA/HCA walkthrough", section 2.3 step 4 and
+# section 5.3: the non-RoPE part of each KV row is quantised to FP8, the RoPE
+# part keeps a wider type). The pages leave the format open; the one used
+# here: e4m3 (OCP FP8: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+# no infinities, S.1111.111 is NaN, largest finite 448) for the first d - rd
+# columns with one float32 scale per row, scale = amax / 448 (1 when the row
+# part is all zero), code = e4m3(x / scale) rounded to nearest even and
+# saturated to +-448; the last rd columns stored as bf16.
+
+def e4m3_decode(codes):
+    """Values of e4m3 codes (uint8 array) as float64."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    val = np.where((e == 0xF) & (m == 0x7), np.nan, val)
+    return sign * val
+
+
+def _e4m3_table():
+    codes = np.arange(0x7F, dtype=np.uint8)  # non-negative finite codes, ascending values
+    return codes, e4m3_decode(codes)
+
+
+def e4m3_encode(x):
+    """Nearest e4m3 code of each value (float64 comparison, ties to the even
+    code), saturating at +-448, the sign kept (also for results of zero);
+    NaN -> 0x7F. A search over the 127 non-negative finite codes, so it does
+    not depend on any bit manipulation."""
+    x = np.asarray(x, dtype=np.float64)
+    codes, vals = _e4m3_table()
+    a = np.abs(x)
+    hi = np.searchsorted(vals, np.minimum(a, 448.0), side="left")  # first value >= a
+    hi = np.clip(hi, 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    dlo = np.abs(a - vals[lo])
+    dhi = np.abs(vals[hi] - a)
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(codes[lo] % 2 == 0, lo, hi)))
+    out = codes[pick].astype(np.uint8)
+    out = np.where(a > 448.0, np.uint8(0x7E), out)
+    out = np.where(np.signbit(x), out | 0x80, out)  # the sign is kept, zeros included
+    out = np.where(np.isnan(x), np.uint8(0x7F), out)
+    return out.astype(np.uint8)
+
+
+def bf16_round(x):
+    """float32 values rounded to bf16 (nearest even), widened back to float32."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    r = ((u + 0x7FFF + lsb) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32)
+
+
+def quantize_kv_fp8(kv, rd):
+    """Split rows kv [..., d] (float32) into (codes uint8 [..., d - rd],
+    rope float32 [..., rd] holding bf16 values, scale float32 [...]).
+    All arithmetic in float32 as stated above."""
+    kv = np.asarray(kv, dtype=np.float32)
+    d = kv.shape[-1]
+    nope, rope = kv[..., :d - rd], kv[..., d - rd:]
+    amax = np.max(np.abs(nope), axis=-1) if d > rd else np.zeros(kv.shape[:-1], np.float32)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    codes = e4m3_encode((nope / scale[..., None]).astype(np.float32))
+    return codes, bf16_round(rope), scale
+
+
+def dequantize_kv_fp8(codes, rope, scale):
+    """Rows [..., d] (float64) from the FP8 layout: e4m3 value x scale for the
+    first d - rd columns, the rope part as stored."""
+    nope = e4m3_decode(codes) * np.asarray(scale, dtype=np.float64)[..., None]
+    return np.concatenate([nope, np.asarray(rope, dtype=np.float64)], axis=-1)
