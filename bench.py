@@ -8,10 +8,10 @@ and both sink semantics (key-0 bias and null logit), four launches of
 sattn_window_fwd over device-resident inputs. The metric is queries/s (query
 tokens per second, all four passes counted).
 
-Other workloads (--workload decode | prefill | block | index | compress)
-measure the gathered decode / prefill path, the chunked block-sparse path,
-the cache bookkeeping (index lists + ring write) and the compressor's gated
-pooling the same way.
+Other workloads (--workload decode | prefill | decode_fp8 | prefill_fp8 |
+block | index | compress) measure the gathered decode / prefill path (bf16 or
+FP8 cache), the chunked block-sparse path, the cache bookkeeping (index lists +
+ring write) and the compressor's gated pooling the same way.
 
 Output: one JSON line on rank 0. Timing: W warm-up steps, then K steps between
 a barrier + device synchronisation on both sides, CUDA events on the launch
@@ -347,8 +347,9 @@ def run_other(args, rank, world, device, peaks, peaks_src):
     stream = torch.cuda.current_stream()
     bf = torch.bfloat16
     seed = rank_seed(rank)
-    if args.workload in ("decode", "prefill"):
-        case = W.sparse_decode_bf16(seed) if args.workload == "decode" else \
+    if args.workload in ("decode", "prefill", "decode_fp8", "prefill_fp8"):
+        fp8 = args.workload.endswith("_fp8")
+        case = W.sparse_decode_bf16(seed) if args.workload.startswith("decode") else \
             W.sparse_prefill_bf16(seed)
         q = torch.from_numpy(case.q).to(bf).to(device)
         kv = torch.from_numpy(case.kv).to(bf).to(device)
@@ -359,18 +360,30 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         nb = sa.sparse_workspace_bytes(case.B, case.M, case.H, case.d, case.K)
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device=device)
         valid = int((case.idx >= 0).sum())
-        nbytes = valid * case.d * 2 + case.idx.size * 4 + 2 * q.numel() * 2 + lse.numel() * 4
+        # a gathered row: 2 d bytes, or (FP8 cache, RoPE half in bf16) d/2 codes +
+        # d bytes of RoPE part + a 4-byte scale
+        row_bytes = (case.d // 2 + case.d + 4) if fp8 else case.d * 2
+        nbytes = valid * row_bytes + case.idx.size * 4 + 2 * q.numel() * 2 + lse.numel() * 4
         flops = 4 * case.d * valid * case.H
         units = case.B * case.M
         # decode is tiny: a scratch buffer larger than L2 is rewritten before every launch
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) \
-            if args.workload == "decode" else None
+            if args.workload.startswith("decode") else None
+        if fp8:
+            kv_nope, kv_rope, kv_scale = sa.quantize_kv_fp8(kv, case.d // 2)
+            del kv
 
         def launch(st=None):
-            sa.sparse_fwd(q, kv, idx, sinks, case.sink_mode, case.scale, o=o, lse=lse,
-                          workspace=ws, stream=st or stream)
-        name = "sparse %s bf16: B=%d M=%d H=%d d=%d N=%d K=%d null_logit" % (
-            args.workload, case.B, case.M, case.H, case.d, case.N, case.K)
+            if fp8:
+                sa.sparse_fp8_fwd(q, kv_nope, kv_rope, kv_scale, idx, sinks, case.sink_mode,
+                                  case.scale, o=o, lse=lse, workspace=ws, stream=st or stream)
+            else:
+                sa.sparse_fwd(q, kv, idx, sinks, case.sink_mode, case.scale, o=o, lse=lse,
+                              workspace=ws, stream=st or stream)
+        name = "sparse %s %s: B=%d M=%d H=%d d=%d N=%d K=%d null_logit" % (
+            args.workload.replace("_fp8", ""),
+            "bf16 q, FP8 cache (e4m3 + row scale, bf16 RoPE half)" if fp8 else "bf16",
+            case.B, case.M, case.H, case.d, case.N, case.K)
     elif args.workload == "index":
         # cache bookkeeping of the prefill layout: index lists of 8192 queries
         # (K = 2048, window 128, ratio 4) and the ring write of the prompt's KV
@@ -448,7 +461,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         launch()
     sa.check_device(stream)
     graph = None
-    if args.workload in ("decode", "index"):
+    if args.workload in ("decode", "decode_fp8", "index"):
         # a step of ~10-30 us of device work is replayed from a CUDA graph so
         # that host-side enqueue time stays out of the timed region
         graph = torch.cuda.CUDAGraph()
@@ -601,7 +614,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="sattn", choices=["sattn", "reference"])
     ap.add_argument("--workload", default="window", choices=["window", "decode", "prefill",
-                                                              "block", "index", "compress"])
+                                                              "block", "index", "compress",
+                                                              "decode_fp8", "prefill_fp8"])
     ap.add_argument("--seqs", type=int, default=256,
                     help="window workload: number of sequences (256 = the full workload)")
     ap.add_argument("--no-e2e", action="store_true")

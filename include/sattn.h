@@ -231,6 +231,44 @@ sattn_status sattn_kv_ring_write(void *kv_cache, const void *kv_new, const int32
                                  sattn_dtype dtype, void *cuda_stream);
 
 /*
+ * FP8 KV cache (DeepSeek-V4 CSA/HCA walkthrough, section 2.3 step 4 and section
+ * 5.3: the non-RoPE part of each KV row is quantised to FP8, the RoPE part keeps
+ * a wider type; the pages leave the format open). Layout used here, per row of
+ * d columns whose last rd are the RoPE part:
+ *   kv_nope uint8 [rows, d - rd]: OCP e4m3 codes of x / scale, round to nearest
+ *     even, saturating at +-448;
+ *   kv_scale float32 [rows]: amax of the row's first d - rd values / 448 (1 when
+ *     they are all zero); value = e4m3(code) * scale;
+ *   kv_rope bf16 [rows, rd]: the last rd values, round to nearest even.
+ *
+ * sattn_quantize_kv_fp8 writes that layout from rows kv [rows, d] (dtype,
+ * device); scale and codes are computed in fp32 with IEEE division.
+ * Requirements: d and rd multiples of 4 with 0 <= rd <= d; all pointers 16-byte
+ * aligned (SATTN_ERR_INVALID_ARG otherwise). Caller-owned buffers.
+ */
+sattn_status sattn_quantize_kv_fp8(const void *kv, uint8_t *kv_nope, void *kv_rope,
+                                   float *kv_scale, int64_t rows, int32_t d, int32_t rd,
+                                   sattn_dtype dtype, void *cuda_stream);
+
+/*
+ * sattn_sparse_fwd over an FP8 cache: the same operation, arguments and
+ * results (q, o bf16), the KV rows of request b being the dequantised rows
+ * b * N .. b * N + N - 1 of the layout above (kv_nope [B, N, d - rd],
+ * kv_scale [B, N], kv_rope [B, N, rd]). The gathered rows are dequantised to
+ * bf16 in shared memory (e4m3 value * scale, rounded to nearest even), so a
+ * gathered row costs d - rd + 2 rd + 4 bytes instead of 2 d.
+ * Supported: H = 32, d = 128, rd = 64 (SATTN_ERR_UNSUPPORTED otherwise);
+ * q, kv_nope, kv_rope and o 16-byte aligned. Workspace as for sattn_sparse_fwd
+ * (sattn_sparse_workspace_bytes).
+ */
+sattn_status sattn_sparse_fp8_fwd(const void *q, const uint8_t *kv_nope, const void *kv_rope,
+                                  const float *kv_scale, const int32_t *topk_idxs,
+                                  const float *sinks, sattn_sink_mode sink_mode, float scale,
+                                  void *o, float *lse, int32_t B, int32_t M, int32_t H, int32_t d,
+                                  int32_t rd, int32_t N, int32_t K, void *workspace,
+                                  size_t workspace_bytes, void *cuda_stream);
+
+/*
  * Compressor gated pooling (DeepSeek-V4 CSA/HCA walkthrough, sections 5.1 and
  * 5.2): every `ratio` consecutive tokens of a sequence become one compressed
  * KV row, the softmax-weighted sum of their kv projections.

@@ -119,6 +119,18 @@ def test_invalid_arguments_rejected_on_host(lib):
                                  64, 8, 4, 1, 0, 0, None) == 1
     assert lib.sattn_compress_kv(None, None, None, None, i64(0), 2, 3, 8, 4, 1, 0, 0,
                                  None) == 0
+    # FP8 layout: rd > d, d not a multiple of 4, misaligned output; gathered
+    # attention over it: unsupported shape, missing scale array
+    assert lib.sattn_quantize_kv_fp8(fake, fake, fake, fake, i64(4), 128, 130, 1, None) == 1
+    assert lib.sattn_quantize_kv_fp8(fake, fake, fake, fake, i64(4), 126, 62, 1, None) == 1
+    assert lib.sattn_quantize_kv_fp8(fake, ctypes.c_void_p(fake.value + 4), fake, fake, i64(4),
+                                     128, 64, 1, None) == 1
+    assert lib.sattn_quantize_kv_fp8(None, None, None, None, i64(0), 128, 64, 1, None) == 0
+    f32 = ctypes.c_float
+    assert lib.sattn_sparse_fp8_fwd(fake, fake, fake, fake, fake, None, 0, f32(0.1), fake, None,
+                                    1, 1, 16, 128, 64, 8, 8, None, 0, None) == 2
+    assert lib.sattn_sparse_fp8_fwd(fake, fake, fake, None, fake, None, 0, f32(0.1), fake, None,
+                                    1, 1, 32, 128, 64, 8, 8, None, 0, None) == 1
 
 
 def test_workspace_size_monotone(lib):

@@ -60,6 +60,11 @@ def lib() -> ctypes.CDLL:
     L.sattn_build_topk_idxs.restype = ctypes.c_int
     L.sattn_kv_ring_write.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_int, P]
     L.sattn_kv_ring_write.restype = ctypes.c_int
+    L.sattn_quantize_kv_fp8.argtypes = [P, P, P, P, i64, i32, i32, ctypes.c_int, P]
+    L.sattn_quantize_kv_fp8.restype = ctypes.c_int
+    L.sattn_sparse_fp8_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_int, f32, P, P, i32, i32, i32,
+                                       i32, i32, i32, i32, P, sz, P]
+    L.sattn_sparse_fp8_fwd.restype = ctypes.c_int
     L.sattn_compress_kv.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, ctypes.c_int,
                                     ctypes.c_int, P]
     L.sattn_compress_kv.restype = ctypes.c_int
@@ -166,6 +171,57 @@ def sparse_fwd(q, kv_cache, topk_idxs, sinks=None, sink_mode=SINK_NONE, scale=No
                                   int(sink_mode), scale, _ptr(o), _ptr(lse), B, M, H, d, N, K,
                                   _ptr(workspace), ws_bytes, _dtype_code(q), _stream(stream))
     _check("sattn_sparse_fwd", code)
+    return o, lse
+
+
+def quantize_kv_fp8(kv, rd, stream=None):
+    """FP8 layout of KV rows (sattn_quantize_kv_fp8): kv [..., d] (bf16 or fp32)
+    -> (codes uint8 [..., d - rd], rope bf16 [..., rd], scale fp32 [...])."""
+    import torch
+
+    _need(kv, "kv", None, kv.device)
+    d = kv.shape[-1]
+    lead = tuple(kv.shape[:-1])
+    rows = kv.numel() // d if d else 0
+    nope = torch.empty(lead + (d - rd,), dtype=torch.uint8, device=kv.device)
+    rope = torch.empty(lead + (rd,), dtype=torch.bfloat16, device=kv.device)
+    scale = torch.empty(lead, dtype=torch.float32, device=kv.device)
+    _check("sattn_quantize_kv_fp8",
+           lib().sattn_quantize_kv_fp8(_ptr(kv), _ptr(nope), _ptr(rope), _ptr(scale), rows, d,
+                                       int(rd), _dtype_code(kv), _stream(stream)))
+    return nope, rope, scale
+
+
+def sparse_fp8_fwd(q, kv_nope, kv_rope, kv_scale, topk_idxs, sinks=None, sink_mode=SINK_NONE,
+                   scale=None, o=None, lse=None, workspace=None, stream=None):
+    """Gathered attention over an FP8 cache (sattn_sparse_fp8_fwd): kv_nope
+    uint8 [B, N, d - rd], kv_rope bf16 [B, N, rd], kv_scale fp32 [B, N].
+    Returns (o, lse)."""
+    import torch
+
+    B, M, H, d = q.shape
+    N, rd = kv_rope.shape[1], kv_rope.shape[2]
+    K = topk_idxs.shape[2]
+    _need(q, "q", torch.bfloat16, q.device)
+    _need(kv_nope, "kv_nope", torch.uint8, q.device)
+    _need(kv_rope, "kv_rope", torch.bfloat16, q.device)
+    _need(kv_scale, "kv_scale", torch.float32, q.device)
+    _need(topk_idxs, "topk_idxs", torch.int32, q.device)
+    if tuple(kv_nope.shape) != (B, N, d - rd) or tuple(kv_scale.shape) != (B, N):
+        raise ValueError("kv_nope must be [B, N, d - rd] and kv_scale [B, N]")
+    if sinks is not None:
+        _need(sinks, "sinks", torch.float32, q.device)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, M, H), dtype=torch.float32, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = float(d ** -0.5 if scale is None else scale)
+    code = lib().sattn_sparse_fp8_fwd(_ptr(q), _ptr(kv_nope), _ptr(kv_rope), _ptr(kv_scale),
+                                      _ptr(topk_idxs), _ptr(sinks), int(sink_mode), scale, _ptr(o),
+                                      _ptr(lse), B, M, H, d, rd, N, K, _ptr(workspace), ws_bytes,
+                                      _stream(stream))
+    _check("sattn_sparse_fp8_fwd", code)
     return o, lse
 
 

@@ -246,15 +246,62 @@ sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t
     const DevInfo *dev = device_info(&e);
     if (!dev) return SATTN_ERR_CUDA;
     if (sattn_status st = check_arch(dev)) return st;
-    SparseArgs a{q, kv_cache, topk_idxs, sink_mode == SATTN_SINK_NONE ? nullptr : sinks,
-                 (int)sink_mode, scale, o, lse, B, M, H, d, N, K, workspace, workspace_bytes,
-                 (int)dtype};
+    SparseArgs a{q, kv_cache, nullptr, nullptr, nullptr, topk_idxs,
+                 sink_mode == SATTN_SINK_NONE ? nullptr : sinks, (int)sink_mode, scale, o, lse,
+                 B, M, H, d, N, K, workspace, workspace_bytes, (int)dtype};
     cudaStream_t s = as_stream(cuda_stream);
     if (dtype == SATTN_BF16) {
         if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(o)) return SATTN_ERR_INVALID_ARG;
         return finish(launch_sparse_tc(a, *dev, s), s);
     }
     return finish(launch_sparse_simt(a, *dev, s), s);
+}
+
+sattn_status sattn_sparse_fp8_fwd(const void *q, const uint8_t *kv_nope, const void *kv_rope,
+                                  const float *kv_scale, const int32_t *topk_idxs,
+                                  const float *sinks, sattn_sink_mode sink_mode, float scale,
+                                  void *o, float *lse, int32_t B, int32_t M, int32_t H, int32_t d,
+                                  int32_t rd, int32_t N, int32_t K, void *workspace,
+                                  size_t workspace_bytes, void *cuda_stream) {
+    if (B < 0 || M < 0 || H <= 0 || N < 0 || K < 0 || d <= 0 || rd < 0 || rd > d)
+        return SATTN_ERR_INVALID_ARG;
+    if (!valid_sink(sink_mode, sinks) || !finite_scale(scale)) return SATTN_ERR_INVALID_ARG;
+    if (B == 0 || M == 0) return SATTN_OK;
+    if (N == 0) return SATTN_ERR_INVALID_ARG;
+    if (!q || !kv_nope || !kv_rope || !kv_scale || !o || (K > 0 && !topk_idxs))
+        return SATTN_ERR_INVALID_ARG;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SATTN_ERR_INVALID_ARG;
+    if (H != 32 || d != 128 || rd != 64) return SATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kv_nope) || !aligned16(kv_rope) || !aligned16(o))
+        return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    SparseArgs a{q, nullptr, kv_nope, kv_rope, kv_scale, topk_idxs,
+                 sink_mode == SATTN_SINK_NONE ? nullptr : sinks, (int)sink_mode, scale, o, lse,
+                 B, M, H, d, N, K, workspace, workspace_bytes, (int)SATTN_BF16};
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_sparse_tc(a, *dev, s), s);
+}
+
+sattn_status sattn_quantize_kv_fp8(const void *kv, uint8_t *kv_nope, void *kv_rope,
+                                   float *kv_scale, int64_t rows, int32_t d, int32_t rd,
+                                   sattn_dtype dtype, void *cuda_stream) {
+    if (rows < 0 || d <= 0 || rd < 0 || rd > d || d % 4 != 0 || rd % 4 != 0 || !valid_dtype(dtype))
+        return SATTN_ERR_INVALID_ARG;
+    if (rows == 0) return SATTN_OK;
+    if (!kv || !kv_nope || !kv_rope || !kv_scale) return SATTN_ERR_INVALID_ARG;
+    if (!aligned16(kv) || !aligned16(kv_nope) || !aligned16(kv_rope) || !aligned16(kv_scale))
+        return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_quantize_kv_fp8(kv, kv_nope, kv_rope, kv_scale, rows, d, rd, (int)dtype,
+                                         *dev, s),
+                  s);
 }
 
 sattn_status sattn_merge_lse(const float *o_parts, const float *lse_parts, int32_t C, int64_t R,

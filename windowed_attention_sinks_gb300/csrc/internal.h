@@ -51,6 +51,11 @@ struct WindowArgs {
 
 struct SparseArgs {
     const void *q, *kv;
+    // FP8 cache (kv == nullptr): e4m3 codes [B, N, d - 64], one fp32 scale per
+    // row, bf16 RoPE part [B, N, 64]
+    const uint8_t *kv_nope;
+    const void *kv_rope;
+    const float *kv_scale;
     const int32_t *idx;
     const float *sinks;
     int sink_mode;
@@ -104,6 +109,9 @@ cudaError_t launch_kv_ring_write(void *cache, const void *src, const int32_t *st
                                  int S, int N, int d, int win, int elem_bytes, const DevInfo &dev,
                                  cudaStream_t s);
 cudaError_t launch_compress_kv(const CompressArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_quantize_kv_fp8(const void *kv, uint8_t *nope, void *rope, float *row_scale,
+                                   long long rows, int d, int rd, int dtype, const DevInfo &dev,
+                                   cudaStream_t s);
 // after_primary: launched as a programmatic dependent of the kernel just
 // issued on `s` (that kernel triggers early; the merge waits for its results).
 cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s,

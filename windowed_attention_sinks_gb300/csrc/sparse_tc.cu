@@ -30,6 +30,7 @@
 // depend on it. With more than one split the normalised partial output and
 // its lse go to the workspace and are merged through their log-sum-exp
 // (sinks added once).
+#include <cuda_fp8.h>
 #include <math.h>
 #include <stdio.h>
 
@@ -110,6 +111,11 @@ static_assert(sizeof(Smem) <= 227 * 1024, "shared memory of one CTA");
 
 struct SpParams {
     const __nv_bfloat16 *q, *kv;
+    // FP8 cache: e4m3 codes of the first DN columns, one scale per row, bf16
+    // RoPE part (the last HD - DN columns)
+    const uint8_t *kv_nope;
+    const __nv_bfloat16 *kv_rope;
+    const float *kv_scale;
     const int32_t *idx;
     const float *sinks;
     int sink_mode;
@@ -224,6 +230,86 @@ struct RowCopier {
     }
 };
 
+// FP8 cache rows: the RoPE part (bf16, the stage's second 64-column half) is
+// copied by cp.async like the bf16 rows; the DN e4m3 codes are loaded to
+// registers before the stage is free, then dequantised (code value x row
+// scale, rounded to bf16) and stored into the first half with the same 128B
+// swizzle.
+constexpr int DN = HD / 2;  // non-RoPE columns
+
+struct Fp8Copier {
+    uint32_t rope_dofs[2];
+    int rsub, ru, rn, cu;
+    // RoPE: lane = (rsub, ru) copies unit ru of rows 4k + rsub (four rows per
+    // instruction); codes: lane = (rn, cu) handles codes 16 cu .. 16 cu + 15 of
+    // rows 8k + rn. A warp's rows start at a multiple of 8, so the swizzle
+    // term of row 4k + rsub is rsub | 4 (k & 1), that of row 8k + rn is rn.
+    __device__ explicit Fp8Copier(int lane) {
+        rsub = lane >> 3;
+        ru = lane & 7;
+        rn = lane >> 2;
+        cu = lane & 3;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            rope_dofs[j] = KV_HALF + (uint32_t)rsub * 128u +
+                           (((uint32_t)ru ^ ((uint32_t)rsub | (4u * j))) << 4);
+    }
+    // codes and scales of this warp's rows (32 g .. 32 g + 31) to registers
+    __device__ void load_codes(const int *ids, const uint8_t *nope, const float *scl, int g,
+                               uint4 (&q)[4], float (&sc)[4]) const {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = ids[32 * g + 8 * k + rn];
+            if (e >= 0) {
+                q[k] = __ldg(reinterpret_cast<const uint4 *>(nope + (size_t)e * DN) + cu);
+                sc[k] = __ldg(scl + e);
+            } else {  // -1 entry: a zero row keeps P V finite
+                q[k] = make_uint4(0u, 0u, 0u, 0u);
+                sc[k] = 0.f;
+            }
+        }
+    }
+    __device__ void issue_rope(uint32_t kv_s, const int *ids, const __nv_bfloat16 *rope,
+                               int g) const {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int e = ids[32 * g + 4 * k + rsub];
+            cp_async16(kv_s + (uint32_t)(32 * g + 4 * k) * 128u + rope_dofs[k & 1],
+                       rope + (size_t)(e >= 0 ? e : 0) * (HD - DN) + ru * 8, e >= 0 ? 16u : 0u);
+        }
+    }
+    // codes -> bf16 (e4m3 value x scale, rounded to nearest even) into the
+    // stage's first half
+    __device__ void store_codes(uint32_t kv_s, int g, const uint4 (&q)[4],
+                                const float (&sc)[4]) const {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const __nv_fp8x2_storage_t two =
+                        (__nv_fp8x2_storage_t)((w[i] >> (16 * hh)) & 0xffffu);
+                    const __half2 h2 = __half2(__nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3));
+                    const float2 f = __half22float2(h2);
+                    o[2 * i + hh] = pack_bf16x2(f.x * sc[k], f.y * sc[k]);
+                }
+            }
+            const uint32_t row = kv_s + (uint32_t)(32 * g + 8 * k + rn) * 128u;
+            const uint32_t a0 = row + ((((uint32_t)(2 * cu)) ^ (uint32_t)rn) << 4);
+            const uint32_t a1 = row + ((((uint32_t)(2 * cu + 1)) ^ (uint32_t)rn) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(o[0]),
+                         "r"(o[1]), "r"(o[2]), "r"(o[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(o[4]),
+                         "r"(o[5]), "r"(o[6]), "r"(o[7])
+                         : "memory");
+        }
+    }
+};
+
 // warp-uniform bounded wait (lane 0 polls)
 __device__ __forceinline__ bool warp_wait(uint64_t &bar, int parity, const DevCtx &ctx,
                                           volatile int *abort) {
@@ -234,20 +320,38 @@ __device__ __forceinline__ bool warp_wait(uint64_t &bar, int parity, const DevCt
     return r != 0;
 }
 
+template <bool FP8>
 __device__ void gather_helper(const SpParams &p, SlotSmem &sm, volatile int *abort, int g,
                               const DevCtx &ctx) {
     SlotBars &b = sm.b;
-    const RowCopier cp(threadIdx.x & 31);
+    const int lane = threadIdx.x & 31;
+    const RowCopier cp(lane);
+    const Fp8Copier fc(lane);
     for (int t = 0;; ++t) {
         const int r = t % IDX_RING, st = t & 1, use = t >> 1;
         if (!warp_wait(b.idx_ready[r], (t / IDX_RING) & 1, ctx, abort)) break;
         const int row0 = sm.tile_row0[r];
         if (row0 < 0) break;
-        if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) break;
-        cp.issue(smem_u32(sm.kv[st]), sm.idx[r], p.kv + (size_t)row0 * HD, g);
-        cp_async_arrive(smem_u32(&b.kv_full[st]));
-        __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&b.idx_empty[r]));
+        if (!FP8) {
+            if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) break;
+            cp.issue(smem_u32(sm.kv[st]), sm.idx[r], p.kv + (size_t)row0 * HD, g);
+            cp_async_arrive(smem_u32(&b.kv_full[st]));
+            __syncwarp();
+        } else {
+            // the codes are loaded before the stage is free (registers only)
+            // the codes are loaded before the stage is free (registers only)
+            uint4 q[4];
+            float sc[4];
+            fc.load_codes(sm.idx[r], p.kv_nope + (size_t)row0 * DN, p.kv_scale + row0, g, q, sc);
+            if (use >= 1 && !warp_wait(b.kv_empty[st], (use - 1) & 1, ctx, abort)) break;
+            fc.issue_rope(smem_u32(sm.kv[st]), sm.idx[r], p.kv_rope + (size_t)row0 * (HD - DN), g);
+            cp_async_arrive(smem_u32(&b.kv_full[st]));
+            fc.store_codes(smem_u32(sm.kv[st]), g, q, sc);
+            fence_proxy_async_smem();  // the stores are read by the tensor core
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&b.kv_full[st]));
+        }
+        if (lane == 0) mbar_arrive(smem_u32(&b.idx_empty[r]));
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
@@ -759,6 +863,10 @@ __device__ void softmax_role(const SpParams &p, SlotSmem &sm, volatile int *abor
     }
 }
 
+// FP8: the cache holds e4m3 codes + scales + bf16 RoPE columns instead of bf16
+// rows (only the copy warps differ; they also arrive once per warp on kv_full
+// after their shared-memory stores)
+template <bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
 sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const DevCtx ctx) {
     extern __shared__ __align__(1024) uint8_t dsmem[];
@@ -772,7 +880,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const
         for (int s = 0; s < NSLOT; ++s) {
             SlotBars &b = all.slot[s].b;
             for (int i = 0; i < 2; ++i) {
-                mbar_init(smem_u32(&b.kv_full[i]), 32 * GATHER_WARPS);  // every copying lane
+                mbar_init(smem_u32(&b.kv_full[i]), 32 * GATHER_WARPS + (FP8 ? GATHER_WARPS : 0));
                 mbar_init(smem_u32(&b.kv_empty[i]), 1);
                 mbar_init(smem_u32(&b.s_full[i]), 1);
                 mbar_init(smem_u32(&b.s_empty[i]), 4);
@@ -816,7 +924,7 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const
         const int role = warp % SLOT_CTRL;  // 0 lead, 1 .. GATHER_WARPS copy, then MMA
         if (role <= GATHER_WARPS) {
             if (role == 0) gather_lead(p, &tq, sm, &all.abort, first, stride, ctx);
-            else gather_helper(p, sm, &all.abort, role - 1, ctx);
+            else gather_helper<FP8>(p, sm, &all.abort, role - 1, ctx);
         } else {
             if ((threadIdx.x & 31) == 0) mma_role(p, sm, &all.abort, tmem, first, stride, ctx);
             __syncwarp();
@@ -859,10 +967,14 @@ size_t sparse_tc_workspace_bytes(int B, int M, int H, int d, int K) {
 }
 
 cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream_t s) {
-    if (a.H != NH || a.d != HD) return launch_sparse_simt(a, dev, s);
+    const bool fp8 = a.kv == nullptr;
+    if (a.H != NH || a.d != HD) return fp8 ? cudaErrorInvalidValue : launch_sparse_simt(a, dev, s);
     SpParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.kv = static_cast<const __nv_bfloat16 *>(a.kv);
+    p.kv_nope = a.kv_nope;
+    p.kv_rope = static_cast<const __nv_bfloat16 *>(a.kv_rope);
+    p.kv_scale = a.kv_scale;
     p.idx = a.idx;
     p.sinks = a.sinks;
     p.sink_mode = a.sink_mode;
@@ -903,18 +1015,19 @@ cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream
             return cudaErrorInvalidValue;
     }
     const size_t smem = sizeof(Smem);
-    static bool attr_set[64] = {};
-    if (!attr_set[dev.device & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(sparse_tc_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = fp8 ? sparse_tc_kernel<true> : sparse_tc_kernel<false>;
+    static bool attr_set[2][64] = {};
+    if (!attr_set[fp8][dev.device & 63]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set[dev.device & 63] = true;
+        attr_set[fp8][dev.device & 63] = true;
     }
     DevCtx ctx{dev.err, wait_limit_ns()};
     if (verbose())
-        fprintf(stderr, "sattn: sparse_tc_kernel grid=%d block=%d smem=%zu items=%lld splits=%d\n",
-                grid, NTHREADS, smem, nitems, splits);
-    sparse_tc_kernel<<<grid, NTHREADS, smem, s>>>(tq, p, ctx);
+        fprintf(stderr, "sattn: sparse_tc_kernel<%s> grid=%d block=%d smem=%zu items=%lld splits=%d\n",
+                fp8 ? "fp8" : "bf16", grid, NTHREADS, smem, nitems, splits);
+    kernel<<<grid, NTHREADS, smem, s>>>(tq, p, ctx);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || splits == 1) return e;
     MergeArgs m{p.o_part, p.lse_part, splits, (int64_t)rows, a.d, a.H,
