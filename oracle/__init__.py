@@ -6,8 +6,9 @@ imports this package. The C source (`sattn_oracle.c`) shares nothing with the
 CUDA implementation.
 
 `topk_idxs` and `kv_ring_write` (cache bookkeeping around the path) are
-plain Python, and `compress_kv` (the compressor's gated pooling) is numpy
-fp64. The attention functions take float32 numpy arrays (the exact input
+plain Python; `compress_kv` (the compressor's gated pooling), the FP8 row
+layout (`e4m3_encode` .. `dequantize_kv_fp8`) and the block-selection stages
+(`xattn_partial_stats` .. `xattn_find_blocks`) are numpy fp64. The attention functions take float32 numpy arrays (the exact input
 values, bf16 inputs widened) and return float64 outputs; each accepts an
 optional `rows` array of row ids so that large workloads can be checked on
 sampled rows:
@@ -337,3 +338,115 @@ def dequantize_kv_fp8(codes, rope, scale):
     first d - rd columns, the rope part as stored."""
     nope = e4m3_decode(codes) * np.asarray(scale, dtype=np.float64)[..., None]
     return np.concatenate([nope, np.asarray(rope, dtype=np.float64)], axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# XAttention block selection ("XAttention Offload Stream Synchronization Fix",
+# technical details: three-stage KV chunking and the block selection step).
+# The estimate here is the exact softmax at full resolution (the pages do not
+# describe a cheaper estimator). numpy fp64.
+
+def _visible(M, q_pos0, j0, j1, causal):
+    """[M, j1 - j0] mask of keys j0 .. j1-1 each query row may see."""
+    i = np.arange(M)[:, None]
+    j = np.arange(j0, j1)[None, :]
+    return (j <= q_pos0 + i) if causal else np.ones((M, j1 - j0), dtype=bool)
+
+
+def xattn_partial_stats(q, k, q_pos0, kv_begin, kv_end, causal, scale):
+    """Stage 1: over the keys j in [kv_begin, kv_end) that query row i may see
+    (j <= q_pos0 + i when causal), per head h: m = max_j s_ij and
+    l = sum_j exp(s_ij - m), with s_ij = scale <q[i, h], k[j, g]> and
+    g = h // (H / Hkv); m = -inf, l = 0 when the row sees none of them.
+    q [M, H, d], k [Nctx, Hkv, d]; returns float64 (m, l), each [M, H]."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    M, H, _ = q.shape
+    group = H // k.shape[1]
+    vis = _visible(M, q_pos0, kv_begin, kv_end, causal)
+    m = np.full((M, H), -np.inf)
+    l = np.zeros((M, H))
+    for h in range(H):
+        s = scale * (q[:, h, :] @ k[kv_begin:kv_end, h // group, :].T)
+        s = np.where(vis, s, -np.inf)
+        if s.shape[1] == 0:
+            continue
+        mh = s.max(axis=1)
+        ok = np.isfinite(mh)
+        e = np.exp(s[ok] - mh[ok, None])
+        m[ok, h] = mh[ok]
+        l[ok, h] = e.sum(axis=1)
+    return m, l
+
+
+def xattn_merge_stats(m_parts, l_parts):
+    """Stage 2: stats of the union of the chunks: m = max_c m_c,
+    l = sum_c l_c exp(m_c - m) (chunks a row sees nothing of add nothing)."""
+    m_parts = np.asarray(m_parts, dtype=np.float64)
+    l_parts = np.asarray(l_parts, dtype=np.float64)
+    m = m_parts.max(axis=0)
+    fin = np.isfinite(m)
+    w = np.where(np.isfinite(m_parts) & fin, np.exp(m_parts - np.where(fin, m, 0.0)), 0.0)
+    l = np.where(fin, (l_parts * w).sum(axis=0), 0.0)
+    return m, l
+
+
+def xattn_block_sum(q, k, m, l, q_pos0, kv_begin, kv_end, causal, scale, blk=128):
+    """Stage 3: softmax probabilities normalised with the global stats (m, l),
+    p_ij = exp(s_ij - m_i) / l_i, summed over blk x blk blocks: entry
+    [h, qb, kb] adds p_ij over rows i in query block qb (i // blk, local) and
+    visible keys j in key block kb (j // blk, absolute) within [kv_begin,
+    kv_end). Returns float64 [H, ceil(M/blk), ceil(Nctx/blk)], zero for key
+    blocks outside the range."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    m = np.asarray(m, dtype=np.float64)
+    l = np.asarray(l, dtype=np.float64)
+    M, H, _ = q.shape
+    Nctx = k.shape[0]
+    group = H // k.shape[1]
+    QB, KB = -(-M // blk), -(-Nctx // blk)
+    out = np.zeros((H, QB, KB))
+    vis = _visible(M, q_pos0, kv_begin, kv_end, causal)
+    for h in range(H):
+        s = scale * (q[:, h, :] @ k[kv_begin:kv_end, h // group, :].T)
+        ok = np.isfinite(m[:, h]) & (l[:, h] > 0)
+        p = np.zeros_like(s)
+        p[ok] = np.exp(s[ok] - m[ok, h, None]) / l[ok, h, None]
+        p = np.where(vis, p, 0.0)
+        kb_of = np.arange(kv_begin, kv_end) // blk
+        qb_of = np.arange(M) // blk
+        for kb in np.unique(kb_of):
+            cols = p[:, kb_of == kb].sum(axis=1)
+            for qb in range(QB):
+                out[h, qb, kb] = cols[qb_of == qb].sum()
+    return out
+
+
+def xattn_find_blocks(block_sum, threshold):
+    """Step 4: for each (head, query block) the key blocks ordered by mass
+    (largest first, the lower block first among equal masses) and the
+    shortest leading run of them whose cumulative mass reaches threshold x
+    the total is selected. Sums in float64, in that order, from the given
+    values (a kernel's fp32 sums reproduce the decisions exactly). Returns
+    uint8 [H, QB, KB]; nothing is selected where the total is not positive."""
+    bs = np.asarray(block_sum)
+    H, QB, KB = bs.shape
+    out = np.zeros((H, QB, KB), dtype=np.uint8)
+    for h in range(H):
+        for qb in range(QB):
+            v = [float(x) for x in bs[h, qb]]
+            order = sorted(range(KB), key=lambda kb: (-v[kb], kb))
+            total = 0.0
+            for kb in order:
+                total += v[kb]
+            if not total > 0.0:
+                continue
+            target = float(threshold) * total
+            cum = 0.0
+            for kb in order:
+                cum += v[kb]
+                out[h, qb, kb] = 1
+                if cum >= target:
+                    break
+    return out
