@@ -269,6 +269,53 @@ sattn_status sattn_sparse_fp8_fwd(const void *q, const uint8_t *kv_nope, const v
                                   size_t workspace_bytes, void *cuda_stream);
 
 /*
+ * XAttention block selection (XAttention Offload Stream Synchronization Fix,
+ * technical details: three-stage KV chunking, then the block selection step).
+ * It produces the block mask that sattn_block_sparse_fwd consumes. The
+ * estimate is the exact softmax at full resolution (the pages describe no
+ * cheaper one). Query rows i = 0 .. M-1 sit at positions q_pos0 + i; key j is
+ * visible to row i iff kv_begin <= j < kv_end and (causal == 0 or
+ * j <= q_pos0 + i). Scores s_ij = scale <q[i, h], k[j, h / (H / Hkv)]>.
+ * Blocks are 128 x 128: query block qb = i / 128 (local), key block
+ * kb = j / 128 (absolute); QB = ceil(M / 128), KB = ceil(Nctx / 128).
+ *   q bf16 [M, H, d], k bf16 [Nctx, Hkv, d] (device, 16-byte aligned).
+ * A chunk [kv_begin, kv_end) must start on a block boundary and end on one or
+ * at Nctx (SATTN_ERR_INVALID_ARG otherwise). Supported: d = 128
+ * (SATTN_ERR_UNSUPPORTED otherwise); scale > 0.
+ *
+ * Stage 1, sattn_xattn_partial_stats: m[i, h] = max of the visible scores of
+ *   the chunk and l[i, h] = sum of exp(s_ij - m) (m = -inf, l = 0 when the row
+ *   sees no key of the chunk); m, l float32 [M, H].
+ * Stage 2, sattn_xattn_merge_stats: m_parts, l_parts float32 [C, R] (R rows,
+ *   e.g. M * H) -> m = max_c m_c, l = sum_c l_c exp(m_c - m).
+ * Stage 3, sattn_xattn_block_sum: with the merged (m, l), block_sum[h, qb, kb]
+ *   = sum over rows i of qb and visible keys j of kb of exp(s_ij - m_i) / l_i,
+ *   written for the chunk's key blocks kb = kv_begin/128 .. ceil(kv_end/128)-1
+ *   (zero for those no row of qb sees); other entries are not touched.
+ *   block_sum float32 [H, QB, KB].
+ * Step 4, sattn_xattn_find_blocks: for each (h, qb) the key blocks ordered by
+ *   block_sum (largest first, the lower kb first among equal values; negative
+ *   values count as 0) and the shortest leading run whose cumulative sum
+ *   (float64, in that order) reaches threshold x their total is selected:
+ *   mask[h, qb, kb] = 1 (uint8 [H, QB, KB]), others 0; nothing where the total
+ *   is 0. Requirements: 0 <= threshold <= 1, KB <= 4096.
+ * All buffers are caller-owned; every call is asynchronous on cuda_stream.
+ */
+sattn_status sattn_xattn_partial_stats(const void *q, const void *k, int32_t M, int32_t Nctx,
+                                       int32_t H, int32_t Hkv, int32_t d, int32_t q_pos0,
+                                       int32_t kv_begin, int32_t kv_end, int32_t causal,
+                                       float scale, float *m, float *l, void *cuda_stream);
+sattn_status sattn_xattn_merge_stats(const float *m_parts, const float *l_parts, int32_t C,
+                                     int64_t R, float *m, float *l, void *cuda_stream);
+sattn_status sattn_xattn_block_sum(const void *q, const void *k, const float *m, const float *l,
+                                   int32_t M, int32_t Nctx, int32_t H, int32_t Hkv, int32_t d,
+                                   int32_t q_pos0, int32_t kv_begin, int32_t kv_end,
+                                   int32_t causal, float scale, float *block_sum,
+                                   void *cuda_stream);
+sattn_status sattn_xattn_find_blocks(const float *block_sum, int32_t H, int32_t QB, int32_t KB,
+                                     float threshold, uint8_t *mask, void *cuda_stream);
+
+/*
  * Compressor gated pooling (DeepSeek-V4 CSA/HCA walkthrough, sections 5.1 and
  * 5.2): every `ratio` consecutive tokens of a sequence become one compressed
  * KV row, the softmax-weighted sum of their kv projections.

@@ -131,6 +131,19 @@ def test_invalid_arguments_rejected_on_host(lib):
                                     1, 1, 16, 128, 64, 8, 8, None, 0, None) == 2
     assert lib.sattn_sparse_fp8_fwd(fake, fake, fake, None, fake, None, 0, f32(0.1), fake, None,
                                     1, 1, 32, 128, 64, 8, 8, None, 0, None) == 1
+    # block selection: chunk not on a block boundary, H % Hkv, d != 128,
+    # threshold out of range
+    assert lib.sattn_xattn_partial_stats(fake, fake, 4, 512, 4, 2, 128, 0, 64, 512, 1, f32(0.1),
+                                         fake, fake, None) == 1
+    assert lib.sattn_xattn_partial_stats(fake, fake, 4, 512, 4, 3, 128, 0, 0, 512, 1, f32(0.1),
+                                         fake, fake, None) == 1
+    assert lib.sattn_xattn_partial_stats(fake, fake, 4, 512, 4, 2, 64, 0, 0, 512, 1, f32(0.1),
+                                         fake, fake, None) == 2
+    assert lib.sattn_xattn_block_sum(fake, fake, fake, fake, 4, 512, 4, 2, 128, 0, 0, 500, 1,
+                                     f32(0.1), fake, None) == 1
+    assert lib.sattn_xattn_find_blocks(fake, 2, 2, 4, f32(1.5), fake, None) == 1
+    assert lib.sattn_xattn_find_blocks(fake, 2, 2, 5000, f32(0.9), fake, None) == 1
+    assert lib.sattn_xattn_merge_stats(None, None, 0, 0, None, None, None) == 0
 
 
 def test_workspace_size_monotone(lib):

@@ -1,0 +1,116 @@
+"""GPU parity of the block-selection stages ("XAttention Offload Stream
+Synchronization Fix", technical details) with the oracle.
+
+Tolerances: partial stats m within 1e-4 (fp32 scores of order 1), l and the
+block sums within 1e-4 relative (sums of ex2-approximated exponentials); the
+selection is compared bit for bit with the oracle's selection run on the
+kernel's own fp32 block sums (the decision is taken in the same precision on
+both sides)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import windowed_attention_sinks_gb300 as sa
+from windowed_attention_sinks_gb300 import workloads as W
+
+from gpu_helpers import dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _qk(seed, M, Nctx, H, Hkv, d=128, qscale=1.0):
+    r = np.random.default_rng(seed)
+    q = W.round_bf16((r.standard_normal((M, H, d)) * qscale).astype(np.float32))
+    k = W.round_bf16(r.standard_normal((Nctx, Hkv, d)).astype(np.float32))
+    return q, k
+
+
+def _cmp_stats(m, l, wm, wl):
+    m, l = m.cpu().numpy(), l.cpu().numpy()
+    assert np.array_equal(np.isneginf(m), np.isneginf(wm))
+    fin = np.isfinite(wm)
+    assert np.abs(m[fin] - wm[fin]).max(initial=0) <= 1e-4
+    assert np.all(l[~fin] == 0)
+    assert np.abs(l[fin] - wl[fin]).max(initial=0) <= 1e-4 * np.abs(wl[fin]).max(initial=1)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("M,Nctx,H,Hkv,q_pos0", [(300, 700, 4, 2, 400), (128, 256, 2, 2, 128),
+                                                 (77, 1000, 3, 1, 923)])
+def test_stats_chunks_and_merge(causal, M, Nctx, H, Hkv, q_pos0):
+    q, k = _qk(M + Nctx, M, Nctx, H, Hkv)
+    scale = 128 ** -0.5
+    qd, kd = dev(q, torch.bfloat16), dev(k, torch.bfloat16)
+    chunks = [(a, min(a + 256, Nctx)) for a in range(0, Nctx, 256)]
+    mp = torch.empty((len(chunks), M, H), device="cuda")
+    lp = torch.empty_like(mp)
+    wparts = []
+    for c, (a, b) in enumerate(chunks):
+        sa.xattn_partial_stats(qd, kd, q_pos0, a, b, causal, scale, m=mp[c], l=lp[c])
+        wparts.append(oracle.xattn_partial_stats(q, k, q_pos0, a, b, causal, scale))
+    sa.check_device()
+    for c in range(len(chunks)):
+        _cmp_stats(mp[c], lp[c], *wparts[c])
+    m, l = sa.xattn_merge_stats(mp, lp)
+    sa.check_device()
+    wm, wl = oracle.xattn_merge_stats([p[0] for p in wparts], [p[1] for p in wparts])
+    _cmp_stats(m, l, wm, wl)
+    # block sums chunk by chunk with the merged stats, then the selection
+    bs = torch.zeros((H, -(-M // 128), -(-Nctx // 128)), device="cuda")
+    for a, b in chunks:
+        sa.xattn_block_sum(qd, kd, m, l, q_pos0, a, b, causal, scale, block_sum=bs)
+    sa.check_device()
+    want = sum(oracle.xattn_block_sum(q, k, wm, wl, q_pos0, a, b, causal, scale) for a, b in chunks)
+    got = bs.cpu().numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-4, atol=1e-5)
+    for thr in (0.5, 0.9, 1.0):
+        mask = sa.xattn_find_blocks(bs, thr).cpu().numpy()
+        assert np.array_equal(mask, oracle.xattn_find_blocks(got, thr)), thr
+
+
+def test_rows_that_see_nothing():
+    # causal rows at positions 0..63 see no key of the chunk [128, 384)
+    q, k = _qk(5, 64, 384, 2, 2)
+    m, l = sa.xattn_partial_stats(dev(q, torch.bfloat16), dev(k, torch.bfloat16), 0, 128, 384,
+                                  True, 0.1)
+    sa.check_device()
+    assert torch.all(torch.isneginf(m)) and torch.all(l == 0)
+
+
+def test_peaked_scores():
+    # sharper softmax (q scaled by 4): the online max moves often within rows
+    q, k = _qk(6, 256, 1024, 2, 1, qscale=4.0)
+    scale = 128 ** -0.5
+    mask, bs = sa.xattn_select_blocks(dev(q, torch.bfloat16), dev(k, torch.bfloat16), 768, True,
+                                      0.9, scale, chunk=512)
+    sa.check_device()
+    wm, wl = oracle.xattn_partial_stats(q, k, 768, 0, 1024, True, scale)
+    want = oracle.xattn_block_sum(q, k, wm, wl, 768, 0, 1024, True, scale)
+    np.testing.assert_allclose(bs.cpu().numpy(), want, rtol=1e-4, atol=1e-5)
+    assert np.array_equal(mask.cpu().numpy(), oracle.xattn_find_blocks(bs.cpu().numpy(), 0.9))
+
+
+def test_full_size_sampled():
+    # the chunked block-sparse workload's shape: the last 4096 positions of a
+    # 32768-token context, 32 heads over 8 KV heads, 4096-key chunks
+    case = W.block_sparse_bf16(0)
+    q, k = case.q, case.k
+    M, H = q.shape[0], q.shape[1]
+    Nctx, Hkv = k.shape[0], k.shape[1]
+    scale = case.scale
+    mask, bs = sa.xattn_select_blocks(dev(q, torch.bfloat16), dev(k, torch.bfloat16), case.q_pos0,
+                                      True, 0.9, scale, chunk=4096)
+    sa.check_device()
+    got = bs.cpu().numpy()
+    rng = np.random.default_rng(0)
+    for h, qb in [(0, 0), (31, 31)] + [tuple(x) for x in rng.integers(0, 32, (4, 2))]:
+        rows = slice(qb * 128, (qb + 1) * 128)
+        g = h // (H // Hkv)
+        q1 = q[rows, h:h + 1]
+        k1 = k[:, g:g + 1]
+        wm, wl = oracle.xattn_partial_stats(q1, k1, case.q_pos0 + qb * 128, 0, Nctx, True, scale)
+        want = oracle.xattn_block_sum(q1, k1, wm, wl, case.q_pos0 + qb * 128, 0, Nctx, True,
+                                      scale)[0, 0]
+        np.testing.assert_allclose(got[h, qb], want, rtol=1e-4, atol=1e-5, err_msg=str((h, qb)))
+    assert np.array_equal(mask.cpu().numpy(), oracle.xattn_find_blocks(got, 0.9))

@@ -65,6 +65,16 @@ def lib() -> ctypes.CDLL:
     L.sattn_sparse_fp8_fwd.argtypes = [P, P, P, P, P, P, ctypes.c_int, f32, P, P, i32, i32, i32,
                                        i32, i32, i32, i32, P, sz, P]
     L.sattn_sparse_fp8_fwd.restype = ctypes.c_int
+    L.sattn_xattn_partial_stats.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                            f32, P, P, P]
+    L.sattn_xattn_partial_stats.restype = ctypes.c_int
+    L.sattn_xattn_merge_stats.argtypes = [P, P, i32, i64, P, P, P]
+    L.sattn_xattn_merge_stats.restype = ctypes.c_int
+    L.sattn_xattn_block_sum.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                        f32, P, P]
+    L.sattn_xattn_block_sum.restype = ctypes.c_int
+    L.sattn_xattn_find_blocks.argtypes = [P, i32, i32, i32, f32, P, P]
+    L.sattn_xattn_find_blocks.restype = ctypes.c_int
     L.sattn_compress_kv.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, ctypes.c_int,
                                     ctypes.c_int, P]
     L.sattn_compress_kv.restype = ctypes.c_int
@@ -327,6 +337,106 @@ def compress_kv(kv, score, ape, ratio, overlap, out=None, out_dtype=None, stream
                                    int(ratio), 1 if overlap else 0, _dtype_code(kv),
                                    _dtype_code(out), _stream(stream)))
     return out
+
+
+def xattn_partial_stats(q, k, q_pos0, kv_begin, kv_end, causal, scale=None, m=None, l=None,
+                        stream=None):
+    """Stage 1 of the block selection over keys [kv_begin, kv_end)
+    (sattn_xattn_partial_stats): q bf16 [M, H, 128], k bf16 [Nctx, Hkv, 128].
+    Returns (m, l), float32 [M, H]."""
+    import torch
+
+    M, H, d = q.shape
+    Nctx, Hkv = k.shape[0], k.shape[1]
+    _need(q, "q", torch.bfloat16, q.device)
+    _need(k, "k", torch.bfloat16, q.device)
+    if m is None:
+        m = torch.empty((M, H), dtype=torch.float32, device=q.device)
+    if l is None:
+        l = torch.empty((M, H), dtype=torch.float32, device=q.device)
+    scale = float(d ** -0.5 if scale is None else scale)
+    _check("sattn_xattn_partial_stats",
+           lib().sattn_xattn_partial_stats(_ptr(q), _ptr(k), M, Nctx, H, Hkv, d, int(q_pos0),
+                                           int(kv_begin), int(kv_end), int(bool(causal)), scale,
+                                           _ptr(m), _ptr(l), _stream(stream)))
+    return m, l
+
+
+def xattn_merge_stats(m_parts, l_parts, m=None, l=None, stream=None):
+    """Stage 2 (sattn_xattn_merge_stats): [C, ...] partial stats -> merged (m, l)."""
+    import torch
+
+    _need(m_parts, "m_parts", torch.float32)
+    _need(l_parts, "l_parts", torch.float32, m_parts.device)
+    C = m_parts.shape[0]
+    R = m_parts[0].numel() if C else 0
+    if m is None:
+        m = torch.empty(m_parts.shape[1:], dtype=torch.float32, device=m_parts.device)
+    if l is None:
+        l = torch.empty(m_parts.shape[1:], dtype=torch.float32, device=m_parts.device)
+    _check("sattn_xattn_merge_stats",
+           lib().sattn_xattn_merge_stats(_ptr(m_parts), _ptr(l_parts), C, R, _ptr(m), _ptr(l),
+                                         _stream(stream)))
+    return m, l
+
+
+def xattn_block_sum(q, k, m, l, q_pos0, kv_begin, kv_end, causal, scale=None, block_sum=None,
+                    stream=None):
+    """Stage 3 (sattn_xattn_block_sum): adds the chunk's key blocks to
+    block_sum float32 [H, ceil(M/128), ceil(Nctx/128)] (zeros if not given)."""
+    import torch
+
+    M, H, d = q.shape
+    Nctx, Hkv = k.shape[0], k.shape[1]
+    _need(q, "q", torch.bfloat16, q.device)
+    _need(k, "k", torch.bfloat16, q.device)
+    _need(m, "m", torch.float32, q.device)
+    _need(l, "l", torch.float32, q.device)
+    if block_sum is None:
+        block_sum = torch.zeros((H, -(-M // BLOCK), -(-Nctx // BLOCK)), dtype=torch.float32,
+                                device=q.device)
+    _need(block_sum, "block_sum", torch.float32, q.device)
+    scale = float(d ** -0.5 if scale is None else scale)
+    _check("sattn_xattn_block_sum",
+           lib().sattn_xattn_block_sum(_ptr(q), _ptr(k), _ptr(m), _ptr(l), M, Nctx, H, Hkv, d,
+                                       int(q_pos0), int(kv_begin), int(kv_end),
+                                       int(bool(causal)), scale, _ptr(block_sum),
+                                       _stream(stream)))
+    return block_sum
+
+
+def xattn_find_blocks(block_sum, threshold, mask=None, stream=None):
+    """Step 4 (sattn_xattn_find_blocks): uint8 mask [H, QB, KB]."""
+    import torch
+
+    _need(block_sum, "block_sum", torch.float32)
+    H, QB, KB = block_sum.shape
+    if mask is None:
+        mask = torch.empty((H, QB, KB), dtype=torch.uint8, device=block_sum.device)
+    _check("sattn_xattn_find_blocks",
+           lib().sattn_xattn_find_blocks(_ptr(block_sum), H, QB, KB, float(threshold), _ptr(mask),
+                                         _stream(stream)))
+    return mask
+
+
+def xattn_select_blocks(q, k, q_pos0, causal, threshold, scale=None, chunk=4096, stream=None):
+    """The whole selection as the pages stage it: partial stats per KV chunk,
+    their merge, block sums per chunk with the merged stats, then the
+    threshold selection. Returns (mask uint8 [H, QB, KB], block_sum)."""
+    import torch
+
+    M, H, _ = q.shape
+    Nctx = k.shape[0]
+    chunks = [(a, min(a + chunk, Nctx)) for a in range(0, Nctx, chunk)] or [(0, 0)]
+    mp = torch.empty((len(chunks), M, H), dtype=torch.float32, device=q.device)
+    lp = torch.empty_like(mp)
+    for c, (a, b) in enumerate(chunks):
+        xattn_partial_stats(q, k, q_pos0, a, b, causal, scale, m=mp[c], l=lp[c], stream=stream)
+    m, l = xattn_merge_stats(mp, lp, stream=stream)
+    bs = torch.zeros((H, -(-M // BLOCK), -(-Nctx // BLOCK)), dtype=torch.float32, device=q.device)
+    for a, b in chunks:
+        xattn_block_sum(q, k, m, l, q_pos0, a, b, causal, scale, block_sum=bs, stream=stream)
+    return xattn_find_blocks(bs, threshold, stream=stream), bs
 
 
 def check_device(stream=None):

@@ -304,6 +304,89 @@ sattn_status sattn_quantize_kv_fp8(const void *kv, uint8_t *kv_nope, void *kv_ro
                   s);
 }
 
+// shared validation of the two estimate passes
+static sattn_status xattn_check(const void *q, const void *k, int32_t M, int32_t Nctx, int32_t H,
+                                int32_t Hkv, int32_t d, int32_t q_pos0, int32_t kv_begin,
+                                int32_t kv_end, int32_t causal, float scale) {
+    if (M < 0 || Nctx < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || q_pos0 < 0)
+        return SATTN_ERR_INVALID_ARG;
+    if (kv_begin < 0 || kv_end > Nctx || kv_begin > kv_end || (causal != 0 && causal != 1))
+        return SATTN_ERR_INVALID_ARG;
+    // chunks cover whole key blocks, so that each block sum comes from one chunk
+    if (kv_begin % 128 != 0 || (kv_end % 128 != 0 && kv_end != Nctx)) return SATTN_ERR_INVALID_ARG;
+    if (!finite_scale(scale)) return SATTN_ERR_INVALID_ARG;
+    if (M > 0 && (!q || (Nctx > 0 && !k))) return SATTN_ERR_INVALID_ARG;
+    if (M > 0 && (!aligned16(q) || (Nctx > 0 && !aligned16(k)))) return SATTN_ERR_INVALID_ARG;
+    if (d != 128) return SATTN_ERR_UNSUPPORTED;
+    return SATTN_OK;
+}
+
+sattn_status sattn_xattn_partial_stats(const void *q, const void *k, int32_t M, int32_t Nctx,
+                                       int32_t H, int32_t Hkv, int32_t d, int32_t q_pos0,
+                                       int32_t kv_begin, int32_t kv_end, int32_t causal,
+                                       float scale, float *m, float *l, void *cuda_stream) {
+    if (sattn_status st = xattn_check(q, k, M, Nctx, H, Hkv, d, q_pos0, kv_begin, kv_end, causal,
+                                      scale))
+        return st;
+    if (M == 0) return SATTN_OK;
+    if (!m || !l) return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    XattnArgs a{q, k, M, Nctx, H, Hkv, q_pos0, kv_begin, kv_end, causal, scale, m, l, nullptr};
+    return finish(launch_xattn_stats(a, *dev, s), s);
+}
+
+sattn_status sattn_xattn_merge_stats(const float *m_parts, const float *l_parts, int32_t C,
+                                     int64_t R, float *m, float *l, void *cuda_stream) {
+    if (C < 0 || R < 0) return SATTN_ERR_INVALID_ARG;
+    if (R == 0) return SATTN_OK;
+    if (!m || !l || (C > 0 && (!m_parts || !l_parts))) return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_xattn_merge_stats(m_parts, l_parts, C, R, m, l, s), s);
+}
+
+sattn_status sattn_xattn_block_sum(const void *q, const void *k, const float *m, const float *l,
+                                   int32_t M, int32_t Nctx, int32_t H, int32_t Hkv, int32_t d,
+                                   int32_t q_pos0, int32_t kv_begin, int32_t kv_end,
+                                   int32_t causal, float scale, float *block_sum,
+                                   void *cuda_stream) {
+    if (sattn_status st = xattn_check(q, k, M, Nctx, H, Hkv, d, q_pos0, kv_begin, kv_end, causal,
+                                      scale))
+        return st;
+    if (M == 0 || kv_begin == kv_end) return SATTN_OK;
+    if (!m || !l || !block_sum) return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    XattnArgs a{q, k, M, Nctx, H, Hkv, q_pos0, kv_begin, kv_end, causal, scale,
+                const_cast<float *>(m), const_cast<float *>(l), block_sum};
+    return finish(launch_xattn_block_sum(a, *dev, s), s);
+}
+
+sattn_status sattn_xattn_find_blocks(const float *block_sum, int32_t H, int32_t QB, int32_t KB,
+                                     float threshold, uint8_t *mask, void *cuda_stream) {
+    if (H < 0 || QB < 0 || KB < 0 || KB > 4096 || !(threshold >= 0.f && threshold <= 1.f))
+        return SATTN_ERR_INVALID_ARG;
+    if ((int64_t)H * QB * KB == 0) return SATTN_OK;
+    if ((int64_t)H * QB > 0x7fffffff) return SATTN_ERR_INVALID_ARG;
+    if (!block_sum || !mask) return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    return finish(launch_xattn_find_blocks(block_sum, H * QB, KB, threshold, mask, s), s);
+}
+
 sattn_status sattn_merge_lse(const float *o_parts, const float *lse_parts, int32_t C, int64_t R,
                              int32_t d, int32_t H, const float *sinks, void *o, float *lse,
                              sattn_dtype dtype, void *cuda_stream) {

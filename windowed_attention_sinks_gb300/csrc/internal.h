@@ -99,6 +99,15 @@ struct CompressArgs {
     int in_dtype, out_dtype;
 };
 
+// Block selection estimate: q [M, H, 128], k [Nctx, Hkv, 128] (bf16).
+struct XattnArgs {
+    const void *q, *k;
+    int M, Nctx, H, Hkv, q_pos0, kv_begin, kv_end, causal;
+    float scale;
+    float *m, *l;      // [M, H]
+    float *block_sum;  // [H, ceil(M/128), ceil(Nctx/128)]
+};
+
 // SIMT kernels: any dtype, d in {64, 128}.
 cudaError_t launch_window_simt(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_sparse_simt(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
@@ -109,6 +118,12 @@ cudaError_t launch_kv_ring_write(void *cache, const void *src, const int32_t *st
                                  int S, int N, int d, int win, int elem_bytes, const DevInfo &dev,
                                  cudaStream_t s);
 cudaError_t launch_compress_kv(const CompressArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_xattn_stats(const XattnArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_xattn_block_sum(const XattnArgs &a, const DevInfo &dev, cudaStream_t s);
+cudaError_t launch_xattn_merge_stats(const float *m_parts, const float *l_parts, int C, long long R,
+                                     float *m_out, float *l_out, cudaStream_t s);
+cudaError_t launch_xattn_find_blocks(const float *block_sum, int rows, int KB, float threshold,
+                                     uint8_t *mask, cudaStream_t s);
 cudaError_t launch_quantize_kv_fp8(const void *kv, uint8_t *nope, void *rope, float *row_scale,
                                    long long rows, int d, int rd, int dtype, const DevInfo &dev,
                                    cudaStream_t s);
