@@ -9,9 +9,10 @@ sattn_window_fwd over device-resident inputs. The metric is queries/s (query
 tokens per second, all four passes counted).
 
 Other workloads (--workload decode | prefill | decode_fp8 | prefill_fp8 |
-block | index | compress) measure the gathered decode / prefill path (bf16 or
-FP8 cache), the chunked block-sparse path, the cache bookkeeping (index lists +
-ring write) and the compressor's gated pooling the same way.
+block | select | index | compress) measure the gathered decode / prefill path
+(bf16 or FP8 cache), the chunked block-sparse path, the block selection that
+produces its mask, the cache bookkeeping (index lists + ring write) and the
+compressor's gated pooling the same way.
 
 Output: one JSON line on rank 0. Timing: W warm-up steps, then K steps between
 a barrier + device synchronisation on both sides, CUDA events on the launch
@@ -403,6 +404,42 @@ def run_other(args, rank, world, device, peaks, peaks_src):
             sa.build_topk_idxs(starts, M, K, win, ratio, out=idx_out, stream=st or stream)
             sa.kv_ring_write(cache, new_kv, starts, win, stream=st or stream)
         name = "cache bookkeeping: topk index lists (8192 queries, K=2048, win 128, ratio 4) + ring write"
+    elif args.workload == "select":
+        # block selection over the chunked block-sparse workload's shape: the
+        # last 4096 positions of a 32768-token context, H=32 over 8 KV heads,
+        # eight 4096-key chunks (stats, merge, block sums, threshold 0.9)
+        nb = 0
+        case = W.block_sparse_bf16(seed)
+        q = torch.from_numpy(case.q).to(bf).to(device)
+        k = torch.from_numpy(case.k).to(bf).to(device)
+        M, H, d = case.q.shape
+        Nctx = case.k.shape[0]
+        chunks = case.chunks
+        mp = torch.empty((len(chunks), M, H), dtype=torch.float32, device=device)
+        lp = torch.empty_like(mp)
+        mm = torch.empty((M, H), dtype=torch.float32, device=device)
+        ll = torch.empty_like(mm)
+        bs = torch.zeros((H, -(-M // 128), -(-Nctx // 128)), dtype=torch.float32, device=device)
+        sel = torch.empty(bs.shape, dtype=torch.uint8, device=device)
+        # visible (row, key) pairs of all heads; each costs one exponential per pass
+        pairs = H * sum(min(Nctx, case.q_pos0 + i + 1) for i in range(M))
+        nbytes = 0
+        flops = 2 * 2 * d * pairs  # QK^T of both passes over the visible pairs
+        units = M
+        flush = None
+
+        def launch(st=None):
+            st = st or stream
+            for c, (a, b) in enumerate(chunks):
+                sa.xattn_partial_stats(q, k, case.q_pos0, a, b, True, case.scale, m=mp[c],
+                                       l=lp[c], stream=st)
+            sa.xattn_merge_stats(mp, lp, m=mm, l=ll, stream=st)
+            for a, b in chunks:
+                sa.xattn_block_sum(q, k, mm, ll, case.q_pos0, a, b, True, case.scale,
+                                   block_sum=bs, stream=st)
+            sa.xattn_find_blocks(bs, 0.9, mask=sel, stream=st)
+        name = ("block selection: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 x 4096-key "
+                "chunks, threshold 0.9")
     elif args.workload == "compress":
         # compressor gated pooling: eight 32K-token prefills at ratio 4 with
         # overlapping windows, fp32 projections in, bf16 rows into the
@@ -492,6 +529,16 @@ def run_other(args, rank, world, device, peaks, peaks_src):
     gbs = nbytes / (ms / 1e3) / 1e9
     tf = flops / (ms / 1e3) / 1e12
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}
+    if args.workload == "select":
+        # one MUFU ex2 per visible (row, key) pair and pass; 16 per clock per
+        # SM (4 per SM sub-partition) at the SM clock sampled during the run
+        clk_mhz = clk.summary().get("sm_mhz") or 2070.0
+        ex2_peak = 16 * torch.cuda.get_device_properties(device).multi_processor_count * \
+            clk_mhz * 1e6 / 1e12
+        ach = 2 * pairs / (ms / 1e3) / 1e12
+        roof = {"bound": "alu", "achieved": ach, "peak": ex2_peak, "unit": "Tex2/s",
+                "frac": ach / ex2_peak}
     unit_name = "compressed rows" if args.workload == "compress" else "queries"
     return {
         "metric": "%s/s (%s)" % (unit_name, args.workload),
@@ -505,8 +552,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                    "l2": "scratch > L2 rewritten before each step" if flush is not None
                    else "inputs larger than L2",
                    "launch": "CUDA graph replay" if graph is not None else "direct"},
-        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
-                     "frac": gbs / peak,
+        "roofline": {**roof,
                      "traffic": profiled_traffic("sparse_tc_kernel<%s>" % args.workload,
                                                  "sparse_tc.cu", units)
                      if args.workload in ("decode", "prefill") else None,
@@ -515,6 +561,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                      "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
         # sparse: the gathered-attention kernel, plus the merge when lists are split
         "gpu_launches": args.steps * (len(case.chunks) + 1 if args.workload == "block"
+                                      else 2 * len(case.chunks) + 2 if args.workload == "select"
                                       else 2 if args.workload == "index" or nb > 0 else 1),
         "clocks": clk.summary(),
     }
@@ -615,7 +662,8 @@ def main():
     ap.add_argument("--impl", default="sattn", choices=["sattn", "reference"])
     ap.add_argument("--workload", default="window", choices=["window", "decode", "prefill",
                                                               "block", "index", "compress",
-                                                              "decode_fp8", "prefill_fp8"])
+                                                              "decode_fp8", "prefill_fp8",
+                                                              "select"])
     ap.add_argument("--seqs", type=int, default=256,
                     help="window workload: number of sequences (256 = the full workload)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -26,8 +26,9 @@ namespace {
 constexpr int BM = 128;  // query rows per CTA
 constexpr int BN = 128;  // keys per tile (= the block size)
 constexpr int HD = 128;
-constexpr int KST = 3;   // key-tile stages
-constexpr int NTHREADS = 192;  // producer, MMA, four reduction warps
+constexpr int KST = 2;   // key-tile stages (two CTAs fit on an SM)
+constexpr int NRED = 8;  // reduction warps: two per TMEM lane quarter, 64 columns each
+constexpr int NTHREADS = 32 * (2 + NRED);  // producer, MMA, reduction warps
 constexpr uint32_t TILE = BM * HD * 2;  // 32 KB
 constexpr uint32_t HALF = TILE / 2;     // one 64-column half
 constexpr int PART = 256;  // tiles whose block partials are kept before a flush
@@ -39,7 +40,7 @@ struct Bars {
 struct alignas(1024) Smem {
     uint8_t q[TILE];
     uint8_t k[KST][TILE];
-    float part[4][PART];  // MODE 3: per reduction warp, per tile: its rows' mass
+    float part[NRED][PART];  // MODE 3: per reduction warp, per tile: its rows' mass
     Bars b;
     uint32_t tmem_base;
     int abort;
@@ -148,30 +149,34 @@ __device__ void mma_thread(Smem &sm, uint32_t tmem, int ntiles, const DevCtx &ct
     mbar_wait(smem_u32(&sm.b.drain), 0, ctx, &zero);
 }
 
-// Named barrier over the 128 reduction threads, OR-reducing a predicate.
+// Named barrier over the reduction threads, OR-reducing a predicate.
 __device__ __forceinline__ int red_bar_or(int pred) {
     int r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.s32 p, %1, 0;\n\t"
-        "bar.red.or.pred q, 1, 128, p;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
         "selp.s32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(pred)
+        : "r"(pred), "r"(32 * NRED)
         : "memory");
     return r;
 }
 
-// One query row per thread (TMEM lane). MODE 1: online (max, sum of exp) of
-// the row's visible scores; MODE 3: the row's mass exp(s - m) / l per tile,
-// summed over the warp's 32 rows, then over the four warps per key block.
+// A query row (TMEM lane) per thread and half-tile: warp w handles lane
+// quarter w % 4 and columns 64 (w / 4) .. +63 of each S tile. MODE 1: online
+// (max, sum of exp) of the row's visible scores, the two halves merged at the
+// end through shared memory; MODE 3: the row's mass exp(s - m) / l per tile,
+// summed over the warp's 32 rows, then over the eight warps per key block.
 template <int MODE>
 __device__ void reduce_rows(const XParams &p, Smem &sm, uint32_t tmem, int qb, int h, Range rg,
                             const DevCtx &ctx) {
     Bars &b = sm.b;
     volatile int *abort = &sm.abort;
     const int lane = threadIdx.x & 31, quarter = (threadIdx.x >> 5) & 3;
-    const int rt = quarter * 32 + lane;  // row within the tile = TMEM lane
+    const int rw = (threadIdx.x >> 5) - 2;  // reduction warp 0 .. NRED-1
+    const int half = rw >> 2;               // column half of the tiles
+    const int rt = quarter * 32 + lane;     // row within the tile = TMEM lane
     const int i = qb * BM + rt;
     const bool row_ok = i < p.M;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -197,22 +202,24 @@ __device__ void reduce_rows(const XParams &p, Smem &sm, uint32_t tmem, int qb, i
         float rowsum = 0.f;
         if (!failed) {
             tc_fence_after();
-            uint32_t v[4][32];
+            uint32_t v[2][32];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) tmem_ld32(tmem + 128u * sb + 32u * cc + lane_off, v[cc]);
+            for (int cc = 0; cc < 2; ++cc)
+                tmem_ld32(tmem + 128u * sb + 64u * half + 32u * cc + lane_off, v[cc]);
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&b.s_empty[sb]));
-            // visible columns of this row: [clo, chi]
-            const int clo = max(0, p.kv_begin - j0), chi = min(BN - 1, jmax - j0);
+            // visible columns of this row within the warp's half: [clo, chi]
+            const int jh = j0 + 64 * half;
+            const int clo = max(0, p.kv_begin - jh), chi = min(63, jmax - jh);
             const bool any = row_ok && chi >= clo && (MODE == 1 || has_mass);
             if (any) {
-                const bool full = clo == 0 && chi == BN - 1;
+                const bool full = clo == 0 && chi == 63;
                 if (MODE == 1) {
                     float mx = -INFINITY;
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc)
+                    for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
                             const int c = 32 * cc + e;
@@ -232,7 +239,7 @@ __device__ void reduce_rows(const XParams &p, Smem &sm, uint32_t tmem, int qb, i
                 const uint64_t off2 = f2_pack(off, off);
                 uint64_t acc_a = f2_pack(0.f, 0.f), acc_b = acc_a;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
+                for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const int c = 32 * cc + e;
@@ -261,14 +268,15 @@ __device__ void reduce_rows(const XParams &p, Smem &sm, uint32_t tmem, int qb, i
             float w = rowsum;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-            if (lane == 0) sm.part[quarter][t - batch0] = w;
+            if (lane == 0) sm.part[rw][t - batch0] = w;
             if (t - batch0 == PART - 1 || t == ntiles - 1) {
                 // every warp reaches this at the same t: the flush is uniform
                 if (red_bar_or(failed)) failed = true;
                 if (!failed) {
-                    for (int tt = rt; tt <= t - batch0; tt += 128) {
-                        const float s = (sm.part[0][tt] + sm.part[1][tt]) +
-                                        (sm.part[2][tt] + sm.part[3][tt]);
+                    for (int tt = rw * 32 + lane; tt <= t - batch0; tt += 32 * NRED) {
+                        float s = 0.f;
+#pragma unroll
+                        for (int w2 = 0; w2 < NRED; ++w2) s += sm.part[w2][tt];
                         p.block_sum[((size_t)h * p.QB + qb) * p.KB + rg.kb_lo + batch0 + tt] = s;
                     }
                 }
@@ -277,20 +285,37 @@ __device__ void reduce_rows(const XParams &p, Smem &sm, uint32_t tmem, int qb, i
             }
         }
     }
-    if (MODE == 1 && row_ok) {
-        p.m[st_idx] = m2 == -INFINITY ? -INFINITY : m2 * LN2;
-        p.l[st_idx] = lsum;
+    if (MODE == 1) {
+        // the two column halves of each row: half 1 hands (m, l) to half 0
+        // (the partial-sum area is free in this mode)
+        float *xm = &sm.part[0][0], *xl = &sm.part[2][0];
+        if (half == 1) {
+            xm[rt] = m2;
+            xl[rt] = lsum;
+        }
+        red_bar_or(0);
+        if (half == 0 && row_ok) {
+            const float mo = xm[rt], lo = xl[rt];
+            const float mn = fmaxf(m2, mo);
+            float l = 0.f;
+            if (mn != -INFINITY) {
+                if (m2 != -INFINITY) l += lsum * ex2(m2 - mn);
+                if (mo != -INFINITY) l += lo * ex2(mo - mn);
+            }
+            p.m[st_idx] = mn == -INFINITY ? -INFINITY : mn * LN2;
+            p.l[st_idx] = l;
+        }
     }
     if (MODE == 3) {
         // key blocks of the chunk that no row of this query block sees
         const int chunk_hi = min(p.KB, (p.kv_end + BN - 1) / BN);
-        for (int kb = rg.kb_hi + rt; kb < chunk_hi; kb += 128)
+        for (int kb = rg.kb_hi + rw * 32 + lane; kb < chunk_hi; kb += 32 * NRED)
             p.block_sum[((size_t)h * p.QB + qb) * p.KB + kb] = 0.f;
     }
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS, 2)
 xattn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                 const XParams p, const DevCtx ctx) {
     extern __shared__ __align__(1024) uint8_t dsmem[];
@@ -311,7 +336,7 @@ xattn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ 
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&b.s_full[i]), 1);
-            mbar_init(smem_u32(&b.s_empty[i]), 4);
+            mbar_init(smem_u32(&b.s_empty[i]), NRED);
         }
         mbar_init(smem_u32(&b.drain), 1);
         sm.abort = 0;
