@@ -215,20 +215,24 @@ __device__ void reduce_rows(const XParams &p, Smem &sm, uint32_t tmem, int qb, i
             const int clo = max(0, p.kv_begin - jh), chi = min(63, jmax - jh);
             const bool any = row_ok && chi >= clo && (MODE == 1 || has_mass);
             if (any) {
-                const bool full = clo == 0 && chi == 63;
+                if (clo != 0 || chi != 63) {
+                    // a boundary tile: invisible scores become -inf once, so
+                    // that the loops below need no tests (ex2(-inf) = 0)
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int c = 32 * cc + e;
+                            if (c < clo || c > chi) v[cc][e] = 0xff800000u;
+                        }
+                }
                 if (MODE == 1) {
                     float mx = -INFINITY;
 #pragma unroll
                     for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const int c = 32 * cc + e;
-                            const float a = (full || (c >= clo && c <= chi))
-                                                ? __uint_as_float(v[cc][e]) : -INFINITY;
-                            const float bb = (full || (c + 1 >= clo && c + 1 <= chi))
-                                                 ? __uint_as_float(v[cc][e + 1]) : -INFINITY;
-                            mx = max3(mx, a, bb);
-                        }
+                        for (int e = 0; e < 32; e += 2)
+                            mx = max3(mx, __uint_as_float(v[cc][e]), __uint_as_float(v[cc][e + 1]));
                     const float mnew = fmaxf(m2, mx * p.scale_l2);  // scale > 0
                     if (mnew > m2) {
                         lsum *= ex2(m2 - mnew);  // ex2(-inf) = 0 on the first tile
@@ -242,19 +246,14 @@ __device__ void reduce_rows(const XParams &p, Smem &sm, uint32_t tmem, int qb, i
                 for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const int c = 32 * cc + e;
                         float x0, x1;
                         f2_unpack(f2_fma(f2_pack(__uint_as_float(v[cc][e]),
                                                  __uint_as_float(v[cc][e + 1])),
                                          c2, off2),
                                   x0, x1);
-                        float e0 = ex2(x0), e1 = ex2(x1);
-                        if (!full) {
-                            if (c < clo || c > chi) e0 = 0.f;
-                            if (c + 1 < clo || c + 1 > chi) e1 = 0.f;
-                        }
-                        if (e & 2) acc_b = f2_add(acc_b, f2_pack(e0, e1));
-                        else acc_a = f2_add(acc_a, f2_pack(e0, e1));
+                        const uint64_t e2 = f2_pack(ex2(x0), ex2(x1));
+                        if (e & 2) acc_b = f2_add(acc_b, e2);
+                        else acc_a = f2_add(acc_a, e2);
                     }
                 float s0, s1;
                 f2_unpack(f2_add(acc_a, acc_b), s0, s1);
