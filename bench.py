@@ -531,10 +531,12 @@ def run_other(args, rank, world, device, peaks, peaks_src):
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}
     if args.workload == "select":
-        # one MUFU ex2 per visible (row, key) pair and pass; 16 per clock per
-        # SM (4 per SM sub-partition) at the SM clock sampled during the run
+        # one MUFU ex2 per visible (row, key) pair and pass; 32 per clock per
+        # SM on this part (twice the rate of the previous generation; an ncu
+        # capture shows the XU pipe about half busy at half this rate) at the
+        # SM clock sampled during the run
         clk_mhz = clk.summary().get("sm_mhz") or 2070.0
-        ex2_peak = 16 * torch.cuda.get_device_properties(device).multi_processor_count * \
+        ex2_peak = 32 * torch.cuda.get_device_properties(device).multi_processor_count * \
             clk_mhz * 1e6 / 1e12
         ach = 2 * pairs / (ms / 1e3) / 1e12
         roof = {"bound": "alu", "achieved": ach, "peak": ex2_peak, "unit": "Tex2/s",
