@@ -192,6 +192,48 @@ __global__ void __launch_bounds__(kWarps * 32) merge_kernel(MergeArgs a) {
     const int lane = threadIdx.x & 31;
     const int64_t r = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (r >= a.R) return;
+    const float sink_v = a.sinks ? __ldg(a.sinks + r % a.H) : -INFINITY;
+    TO *orow_v = static_cast<TO *>(a.o) + r * a.d;
+    if (a.C <= 32 && (a.d & 3) == 0 && a.d <= 128 &&
+        (reinterpret_cast<uintptr_t>(a.o_parts) & 15u) == 0) {
+        // lane c holds split c's lse (one load); each lane owns four
+        // consecutive columns and reads them from every split with one
+        // 16-byte load; splits with nothing (lse = -inf) are skipped
+        const float lc = lane < a.C ? __ldg(a.lse_parts + (int64_t)lane * a.R + r) : -INFINITY;
+        const float m = fmaxf(warp_max(lc), sink_v);
+        const int col = 4 * lane;
+        if (m == -INFINITY) {
+            if (col < a.d) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) orow_v[col + k] = from_f32<TO>(0.0f);
+            }
+            if (a.lse && lane == 0) a.lse[r] = -INFINITY;
+            return;
+        }
+        float z = warp_sum(lc == -INFINITY ? 0.f : ex2((lc - m) * LOG2E));
+        if (a.sinks) z += ex2((sink_v - m) * LOG2E);
+        const float L = m + logf(z);
+        const float w = lc == -INFINITY ? 0.f : ex2((lc - L) * LOG2E);
+        const unsigned live = __ballot_sync(0xffffffffu, lc != -INFINITY);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+        for (int c = 0; c < a.C; ++c) {
+            const float wc = __shfl_sync(0xffffffffu, w, c);
+            if (!((live >> c) & 1u) || col >= a.d) continue;
+            const float4 v = __ldg(
+                reinterpret_cast<const float4 *>(a.o_parts + ((int64_t)c * a.R + r) * a.d + col));
+            acc[0] += wc * v.x;
+            acc[1] += wc * v.y;
+            acc[2] += wc * v.z;
+            acc[3] += wc * v.w;
+        }
+        if (col < a.d) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) orow_v[col + k] = from_f32<TO>(acc[k]);
+        }
+        if (a.lse && lane == 0) a.lse[r] = L;
+        return;
+    }
     float m = -INFINITY;
     for (int c = lane; c < a.C; c += 32) m = fmaxf(m, __ldg(a.lse_parts + (int64_t)c * a.R + r));
     m = warp_max(m);
