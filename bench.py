@@ -486,11 +486,22 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         units = case.M
         flush = None
 
+        side = torch.cuda.Stream(device=device)
+        ev_go, ev_done = torch.cuda.Event(), torch.cuda.Event()
+
         def launch(st=None):
+            # the chunks are independent: they alternate between two streams,
+            # so that a chunk's grid fills the SMs the previous one's tail
+            # leaves idle; the merge waits for both
+            ev_go.record(stream)
+            side.wait_event(ev_go)
             for c, (a, b) in enumerate(case.chunks):
                 sa.block_sparse_fwd(q, k, v, mask, case.q_pos0, a, b, True, case.scale,
                                     o_part=op[c].view(case.M, case.H, case.d),
-                                    lse_part=lp[c].view(case.M, case.H), stream=stream)
+                                    lse_part=lp[c].view(case.M, case.H),
+                                    stream=stream if c % 2 == 0 else side)
+            ev_done.record(side)
+            stream.wait_event(ev_done)
             sa.merge_lse(op, lp, case.H, o=o, lse=lse, stream=stream)
         name = "block-sparse bf16: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 chunks + merge"
 
