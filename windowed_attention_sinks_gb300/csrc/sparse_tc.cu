@@ -446,6 +446,7 @@ __device__ void gather_lead(const SpParams &p, const CUtensorMap *tq, SlotSmem &
             break;
         }
         q_pend = it.bm;
+        issue_q(false);  // at once when the buffer is free (always for the first item)
         int ring = gt % IDX_RING;  // ring entry of the tile being compacted
         // Publish and issue the compacted tile gt holding `pos` rows.
         auto close_tile = [&](int pos, bool last) -> bool {
