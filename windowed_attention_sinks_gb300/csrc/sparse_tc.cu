@@ -14,15 +14,20 @@
 // are split across CTAs). A persistent grid of one CTA per SM runs two
 // independent slots, each with its own shared memory, TMEM columns,
 // barriers and item stream. Each slot is warp-specialised:
-//   lead warp     loads Q (TMA) and compacts the valid list entries
+//   lead warp     streams the index lists into shared memory (bulk copies
+//                 of 256-entry chunks), compacts the valid entries
 //                 (0 <= idx < N) into tiles of up to 128 rows, so -1 entries
-//                 cost no MMA work; tiles go through a 3-entry ring.
+//                 cost no MMA work, and publishes them through a 5-entry
+//                 ring that every reader releases; loads Q (TMA) as soon as
+//                 the slot's Q buffer is free.
 //   copy warps    copy each tile's rows with 16-byte cp.async into a
 //                 128B-swizzled K-major stage (rows past the count are
-//                 zero-filled); two stages, completed on an mbarrier.
-//   MMA thread    S^T of tile t into one of two S buffers, then
-//                 O^T += KV^T P^T for tile t-1, so the tensor core works on
-//                 the next scores while the softmax runs.
+//                 zero-filled); two stages, completed on an mbarrier. With
+//                 an FP8 cache they take the bf16 RoPE half by cp.async and
+//                 dequantise the e4m3 half into the stage.
+//   MMA thread    issues in readiness order: S^T of the next tile into one
+//                 of two S buffers as soon as its rows have landed, and
+//                 O^T += KV^T P^T of a tile as soon as its P is written.
 //   4 warps       softmax, one head per lane after a per-warp transpose;
 //                 running max / sum per head in the log2 domain, P (bf16)
 //                 to a double-buffered shared tile; epilogue O^T / l.
