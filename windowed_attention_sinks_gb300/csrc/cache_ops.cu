@@ -9,25 +9,29 @@
 namespace sattn {
 namespace {
 
-// One thread per 16 consecutive entries of one query's list (four int4
-// stores when K % 4 == 0). Integer work is hoisted out of the entries: with
+// A warp writes 512 consecutive entries of one query's list: lane l takes
+// the groups of four entries l, l + 32, l + 64, l + 96 of that span, so every
+// store instruction of the warp covers 512 contiguous bytes (int4 stores when
+// K % 4 == 0). Integer work is hoisted out of the entries: with
 // base = (p + 1) mod win, window slot k (token t = p - win + 1 + k >= 0) sits
 // at ring row (base + k) mod win, a single conditional subtraction.
-constexpr int ENTRIES = 16;
+constexpr int GROUPS = 4;              // groups of four entries per thread
+constexpr int SPAN = 32 * 4 * GROUPS;  // entries per warp
 
 __global__ void topk_idxs_kernel(int32_t *__restrict__ out, const int32_t *__restrict__ start_pos,
-                                 int M, int K, int win, int ratio, int per_row, int total,
+                                 int M, int K, int win, int ratio, int warps_per_row, int total,
                                  DevCtx ctx) {
     const int g = blockIdx.x * blockDim.x + threadIdx.x;
     if (g >= total) return;
-    const int row = g / per_row;  // (b, m)
-    const int k0 = (g - row * per_row) * ENTRIES;
+    const int w = g >> 5, lane = g & 31;
+    const int row = w / warps_per_row;  // (b, m)
+    const int kw = (w - row * warps_per_row) * SPAN;
     const int b = row / M, m = row - b * M;
     const int sp = __ldg(start_pos + b);
     // positions are 0 .. 2^31 - 2 (32-bit arithmetic below); others leave the
     // lists at -1 and are reported
     const bool ok = sp >= 0 && sp <= 0x7ffffffe - m;
-    if (!ok && k0 == 0) record_error(ctx, DEVERR_INDEX);
+    if (!ok && kw == 0 && lane == 0) record_error(ctx, DEVERR_INDEX);
     const unsigned p = ok ? (unsigned)(sp + m) : 0u;  // absolute position
     const int base = (int)((p + 1u) % (unsigned)win);
     const long long first_t = (long long)p - win + 1;  // token of window slot 0
@@ -36,30 +40,31 @@ __global__ void topk_idxs_kernel(int32_t *__restrict__ out, const int32_t *__res
     const int room = K - win;
     const int first_c = visible > room ? visible - room : 0;
     const int ncomp = visible - first_c;
-    int v[ENTRIES];
+    int32_t *dst = out + (long long)row * K;
 #pragma unroll
-    for (int e = 0; e < ENTRIES; ++e) {
-        const int k = k0 + e;
-        int x = -1;
-        if (ok) {
-            if (k < win) {
-                if (first_t + k >= 0) x = base + k < win ? base + k : base + k - win;
-            } else if (k - win < ncomp) {
-                x = win + first_c + (k - win);
+    for (int j = 0; j < GROUPS; ++j) {
+        const int k0 = kw + 4 * (lane + 32 * j);
+        int v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k = k0 + e;
+            int x = -1;
+            if (ok) {
+                if (k < win) {
+                    if (first_t + k >= 0) x = base + k < win ? base + k : base + k - win;
+                } else if (k - win < ncomp) {
+                    x = win + first_c + (k - win);
+                }
             }
+            v[e] = x;
         }
-        v[e] = x;
-    }
-    int32_t *dst = out + (long long)row * K + k0;
-    if ((K & 3) == 0) {
+        if ((K & 3) == 0) {
+            if (k0 < K) *reinterpret_cast<int4 *>(dst + k0) = make_int4(v[0], v[1], v[2], v[3]);
+        } else {
 #pragma unroll
-        for (int e = 0; e < ENTRIES; e += 4)
-            if (k0 + e < K)
-                *reinterpret_cast<int4 *>(dst + e) = make_int4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-    } else {
-#pragma unroll
-        for (int e = 0; e < ENTRIES; ++e)
-            if (k0 + e < K) dst[e] = v[e];
+            for (int e = 0; e < 4; ++e)
+                if (k0 + e < K) dst[k0 + e] = v[e];
+        }
     }
 }
 
@@ -90,14 +95,14 @@ __global__ void ring_write_kernel(uint8_t *__restrict__ cache, const uint8_t *__
 
 cudaError_t launch_topk_idxs(int32_t *out, const int32_t *start_pos, int B, int M, int K, int win,
                              int ratio, const DevInfo &dev, cudaStream_t s) {
-    const int per_row = (K + ENTRIES - 1) / ENTRIES;
-    const long long total = (long long)B * M * per_row;
+    const int warps_per_row = (K + SPAN - 1) / SPAN;
+    const long long total = (long long)B * M * warps_per_row * 32;
     if (total == 0) return cudaSuccess;
     if (total > 0x7fffffffLL - 256) return cudaErrorInvalidValue;  // 32-bit thread index
     const int threads = 256;
     const int blocks = (int)((total + threads - 1) / threads);
     DevCtx ctx{dev.err, wait_limit_ns()};
-    topk_idxs_kernel<<<blocks, threads, 0, s>>>(out, start_pos, M, K, win, ratio, per_row,
+    topk_idxs_kernel<<<blocks, threads, 0, s>>>(out, start_pos, M, K, win, ratio, warps_per_row,
                                                 (int)total, ctx);
     return cudaGetLastError();
 }
