@@ -126,3 +126,14 @@ def test_matches_bf16_path_on_exact_rows():
                              case.scale, workspace=ws)
     sa.check_device()
     assert torch.equal(o8, o16) and torch.equal(l8, l16)
+
+
+def test_lists_of_only_invalid_entries():
+    # every entry -1: o = 0 and lse = the sink (null logit) for every head
+    case = W.sparse_decode_bf16(7, B=3)
+    case.idx[...] = -1
+    codes, rope, scale, deq = _fp8_cache(case)
+    o, lse = run_fp8(case, codes, rope, scale)
+    assert torch.all(o == 0)
+    np.testing.assert_allclose(lse.cpu().numpy(),
+                               np.broadcast_to(case.sinks, lse.shape), rtol=0, atol=1e-5)

@@ -114,3 +114,28 @@ def test_full_size_sampled():
                                       scale)[0, 0]
         np.testing.assert_allclose(got[h, qb], want, rtol=1e-4, atol=1e-5, err_msg=str((h, qb)))
     assert np.array_equal(mask.cpu().numpy(), oracle.xattn_find_blocks(got, 0.9))
+
+
+@pytest.mark.parametrize("M,Nctx,q_pos0", [(5, 60, 55), (128, 100, 0), (40, 130, 90)])
+def test_tiny_and_partial_blocks(M, Nctx, q_pos0):
+    # fewer rows than a query block, fewer keys than a key block, ragged tails
+    q, k = _qk(7 + M, M, Nctx, 2, 1)
+    scale = 128 ** -0.5
+    mask, bs = sa.xattn_select_blocks(dev(q, torch.bfloat16), dev(k, torch.bfloat16), q_pos0,
+                                      True, 0.9, scale, chunk=128)
+    sa.check_device()
+    wm, wl = oracle.xattn_partial_stats(q, k, q_pos0, 0, Nctx, True, scale)
+    want = oracle.xattn_block_sum(q, k, wm, wl, q_pos0, 0, Nctx, True, scale)
+    np.testing.assert_allclose(bs.cpu().numpy(), want, rtol=1e-4, atol=1e-5)
+    assert np.array_equal(mask.cpu().numpy(), oracle.xattn_find_blocks(bs.cpu().numpy(), 0.9))
+
+
+def test_empty_chunk_leaves_stats_empty_and_sums_untouched():
+    q, k = _qk(8, 64, 256, 2, 2)
+    qd, kd = dev(q, torch.bfloat16), dev(k, torch.bfloat16)
+    m, l = sa.xattn_partial_stats(qd, kd, 200, 128, 128, True, 0.1)
+    bs = torch.full((2, 1, 2), 5.0, device="cuda")
+    sa.xattn_block_sum(qd, kd, m, l, 200, 128, 128, True, 0.1, block_sum=bs)
+    sa.check_device()
+    assert torch.all(torch.isneginf(m)) and torch.all(l == 0)
+    assert torch.all(bs == 5.0)
