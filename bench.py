@@ -444,12 +444,10 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         k = torch.from_numpy(case.k).to(bf).to(device)
         M, H, d = case.q.shape
         Nctx = case.k.shape[0]
-        chunks = case.chunks
-        mp = torch.empty((len(chunks), M, H), dtype=torch.float32, device=device)
-        lp = torch.empty_like(mp)
-        mm = torch.empty((M, H), dtype=torch.float32, device=device)
-        ll = torch.empty_like(mm)
-        bs = torch.zeros((H, -(-M // 128), -(-Nctx // 128)), dtype=torch.float32, device=device)
+        chunk = case.chunks[0][1] - case.chunks[0][0]
+        ws = torch.empty(sa.xattn_select_workspace_bytes(M, H, Nctx, chunk), dtype=torch.uint8,
+                         device=device)
+        bs = torch.empty((H, -(-M // 128), -(-Nctx // 128)), dtype=torch.float32, device=device)
         sel = torch.empty(bs.shape, dtype=torch.uint8, device=device)
         # visible (row, key) pairs of all heads; each costs one exponential per pass
         pairs = H * sum(min(Nctx, case.q_pos0 + i + 1) for i in range(M))
@@ -459,17 +457,11 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         flush = None
 
         def launch(st=None):
-            st = st or stream
-            for c, (a, b) in enumerate(chunks):
-                sa.xattn_partial_stats(q, k, case.q_pos0, a, b, True, case.scale, m=mp[c],
-                                       l=lp[c], stream=st)
-            sa.xattn_merge_stats(mp, lp, m=mm, l=ll, stream=st)
-            for a, b in chunks:
-                sa.xattn_block_sum(q, k, mm, ll, case.q_pos0, a, b, True, case.scale,
-                                   block_sum=bs, stream=st)
-            sa.xattn_find_blocks(bs, 0.9, mask=sel, stream=st)
+            # stats of all chunks, merge, block sums, threshold 0.9: four launches
+            sa.xattn_select_blocks(q, k, case.q_pos0, True, 0.9, case.scale, chunk=chunk,
+                                   workspace=ws, block_sum=bs, mask=sel, stream=st or stream)
         name = ("block selection: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 x 4096-key "
-                "chunks, threshold 0.9")
+                "chunks, threshold 0.9, one call")
     elif args.workload == "compress":
         # compressor gated pooling: eight 32K-token prefills at ratio 4 with
         # overlapping windows, fp32 projections in, bf16 rows into the
@@ -572,16 +564,19 @@ def run_other(args, rank, world, device, peaks, peaks_src):
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}
     if args.workload == "select":
-        # one MUFU ex2 per visible (row, key) pair and pass; 32 per clock per
-        # SM on this part (twice the rate of the previous generation; an ncu
-        # capture shows the XU pipe about half busy at half this rate) at the
-        # SM clock sampled during the run
+        # S = Q K^T of both passes over the visible (row, key) pairs against
+        # the measured bf16 tensor peak, the tighter of the two bounds; beside
+        # it the exponential unit: one MUFU ex2 per visible pair and pass, 32
+        # per clock per SM on this part at the SM clock sampled during the run
         clk_mhz = clk.summary().get("sm_mhz") or 2070.0
         ex2_peak = 32 * torch.cuda.get_device_properties(device).multi_processor_count * \
             clk_mhz * 1e6 / 1e12
-        ach = 2 * pairs / (ms / 1e3) / 1e12
-        roof = {"bound": "alu", "achieved": ach, "peak": ex2_peak, "unit": "Tex2/s",
-                "frac": ach / ex2_peak}
+        ex2 = 2 * pairs / (ms / 1e3) / 1e12
+        tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": tf / tpeak,
+                "ex2": {"achieved": ex2, "peak": ex2_peak, "unit": "Tex2/s",
+                        "frac": ex2 / ex2_peak}}
     unit_name = "compressed rows" if args.workload == "compress" else "queries"
     return {
         "metric": "%s/s (%s)" % (unit_name, args.workload),
@@ -604,7 +599,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                      "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
         # sparse: the gathered-attention kernel, plus the merge when lists are split
         "gpu_launches": args.steps * (len(case.chunks) + 1 if args.workload == "block"
-                                      else 2 * len(case.chunks) + 2 if args.workload == "select"
+                                      else 4 if args.workload == "select"
                                       else 2 if args.workload == "index" or nb > 0 else 1),
         "clocks": clk.summary(),
     }

@@ -280,7 +280,7 @@ sattn_status sattn_sparse_fp8_fwd(const void *q, const uint8_t *kv_nope, const v
  * kb = j / 128 (absolute); QB = ceil(M / 128), KB = ceil(Nctx / 128).
  *   q bf16 [M, H, d], k bf16 [Nctx, Hkv, d] (device, 16-byte aligned).
  * A chunk [kv_begin, kv_end) must start on a block boundary and end on one or
- * at Nctx (SATTN_ERR_INVALID_ARG otherwise). Supported: d = 128
+ * at Nctx (SATTN_ERR_INVALID_ARG otherwise); H <= 65535. Supported: d = 128
  * (SATTN_ERR_UNSUPPORTED otherwise); scale > 0.
  *
  * Stage 1, sattn_xattn_partial_stats: m[i, h] = max of the visible scores of
@@ -314,6 +314,29 @@ sattn_status sattn_xattn_block_sum(const void *q, const void *k, const float *m,
                                    void *cuda_stream);
 sattn_status sattn_xattn_find_blocks(const float *block_sum, int32_t H, int32_t QB, int32_t KB,
                                      float threshold, uint8_t *mask, void *cuda_stream);
+
+/*
+ * The four steps in one call over the whole key range [0, Nctx): stage 1 for
+ * the C = ceil(Nctx / chunk) chunks [c chunk, min(Nctx, (c + 1) chunk)) in
+ * one launch, stage 2 over those C partial stats, stage 3 over [0, Nctx),
+ * step 4. The results are those of the four calls above made chunk by chunk,
+ * bit for bit. Four kernel launches in all.
+ *   chunk: a positive multiple of 128 with C <= 65535 (SATTN_ERR_INVALID_ARG
+ *     otherwise); KB <= 4096.
+ *   workspace: a caller-owned device buffer of at least
+ *     sattn_xattn_select_workspace_bytes(M, H, Nctx, chunk) bytes, 16-byte
+ *     aligned; it receives the per-chunk stats and the merged stats (float32
+ *     [2 C + 2, M, H]) and is free again when the call's work has run.
+ *   block_sum float32 [H, QB, KB] and mask uint8 [H, QB, KB]: every entry is
+ *     written.
+ * M == 0 or Nctx == 0: nothing to do (SATTN_OK).
+ */
+size_t sattn_xattn_select_workspace_bytes(int32_t M, int32_t H, int32_t Nctx, int32_t chunk);
+sattn_status sattn_xattn_select_blocks(const void *q, const void *k, int32_t M, int32_t Nctx,
+                                       int32_t H, int32_t Hkv, int32_t d, int32_t q_pos0,
+                                       int32_t causal, float scale, int32_t chunk,
+                                       float threshold, void *workspace, size_t workspace_bytes,
+                                       float *block_sum, uint8_t *mask, void *cuda_stream);
 
 /*
  * Compressor gated pooling (DeepSeek-V4 CSA/HCA walkthrough, sections 5.1 and

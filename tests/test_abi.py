@@ -144,6 +144,30 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.sattn_xattn_find_blocks(fake, 2, 2, 4, f32(1.5), fake, None) == 1
     assert lib.sattn_xattn_find_blocks(fake, 2, 2, 5000, f32(0.9), fake, None) == 1
     assert lib.sattn_xattn_merge_stats(None, None, 0, 0, None, None, None) == 0
+    # the one-call selection: chunk not a multiple of 128 or 0, threshold out
+    # of range, workspace too small or misaligned, too many key blocks, more
+    # heads than a grid dimension holds; no rows is no work
+    ws = lib.sattn_xattn_select_workspace_bytes(256, 4, 1024, 256)
+
+    def sel(M=256, Nctx=1024, H=4, chunk=256, thr=0.9, w=fake, nb=ws):
+        return lib.sattn_xattn_select_blocks(fake, fake, M, Nctx, H, 2, 128, 0, 1, f32(0.1), chunk,
+                                             f32(thr), w, nb, fake, fake, None)
+    assert sel(chunk=200) == 1
+    assert sel(chunk=0) == 1
+    assert sel(thr=1.5) == 1
+    assert sel(nb=ws - 4) == 1
+    assert sel(w=ctypes.c_void_p(fake.value + 8)) == 1
+    assert sel(Nctx=4097 * 128, chunk=128 * 4097) == 1
+    assert sel(H=65536 * 2) == 1
+    assert sel(M=0, w=None, nb=0) == 0
+
+
+def test_select_workspace_bytes(lib):
+    # per-chunk (m, l) and the merged (m, l), float32 [2 C + 2, M, H]
+    assert lib.sattn_xattn_select_workspace_bytes(256, 4, 1024, 256) == (2 * 4 + 2) * 256 * 4 * 4
+    assert lib.sattn_xattn_select_workspace_bytes(100, 3, 1000, 384) == (2 * 3 + 2) * 100 * 3 * 4
+    assert lib.sattn_xattn_select_workspace_bytes(0, 4, 1024, 256) == 0
+    assert lib.sattn_xattn_select_workspace_bytes(256, 4, 1024, 0) == 0
 
 
 def test_workspace_size_monotone(lib):

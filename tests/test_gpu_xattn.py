@@ -139,3 +139,51 @@ def test_empty_chunk_leaves_stats_empty_and_sums_untouched():
     sa.check_device()
     assert torch.all(torch.isneginf(m)) and torch.all(l == 0)
     assert torch.all(bs == 5.0)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("M,Nctx,H,Hkv,q_pos0,chunk", [(300, 5000, 4, 2, 4700, 1024),
+                                                       (200, 700, 3, 3, 500, 256),
+                                                       (129, 9000, 6, 2, 8871, 4096),
+                                                       (64, 4224, 8, 1, 4160, 640)])
+def test_one_call_equals_the_stages(causal, M, Nctx, H, Hkv, q_pos0, chunk):
+    # the one-call selection (stage 1 over all chunks in one launch, stage 3
+    # over 4096-key pieces) reproduces the four stage calls made chunk by
+    # chunk, bit for bit; groups of 1, 2, 3 and 8 heads per KV head
+    q, k = _qk(11 + M, M, Nctx, H, Hkv)
+    scale = 128 ** -0.5
+    qd, kd = dev(q, torch.bfloat16), dev(k, torch.bfloat16)
+    mask, bs = sa.xattn_select_blocks(qd, kd, q_pos0, causal, 0.9, scale, chunk=chunk)
+    chunks = [(a, min(a + chunk, Nctx)) for a in range(0, Nctx, chunk)]
+    mp = torch.empty((len(chunks), M, H), device="cuda")
+    lp = torch.empty_like(mp)
+    for c, (a, b) in enumerate(chunks):
+        sa.xattn_partial_stats(qd, kd, q_pos0, a, b, causal, scale, m=mp[c], l=lp[c])
+    m, l = sa.xattn_merge_stats(mp, lp)
+    bs2 = torch.full_like(bs, float("nan"))
+    for a, b in chunks:
+        sa.xattn_block_sum(qd, kd, m, l, q_pos0, a, b, causal, scale, block_sum=bs2)
+    mask2 = sa.xattn_find_blocks(bs2, 0.9)
+    sa.check_device()
+    assert torch.equal(bs, bs2) and torch.equal(mask, mask2)
+    # and the oracle on the whole range
+    wm, wl = oracle.xattn_partial_stats(q, k, q_pos0, 0, Nctx, causal, scale)
+    want = oracle.xattn_block_sum(q, k, wm, wl, q_pos0, 0, Nctx, causal, scale)
+    np.testing.assert_allclose(bs.cpu().numpy(), want, rtol=1e-4, atol=1e-5)
+
+
+def test_one_call_reuses_caller_buffers():
+    q, k = _qk(12, 256, 2048, 4, 2)
+    qd, kd = dev(q, torch.bfloat16), dev(k, torch.bfloat16)
+    ws = torch.empty(sa.xattn_select_workspace_bytes(256, 4, 2048, 512), dtype=torch.uint8,
+                     device="cuda")
+    bs = torch.full((4, 2, 16), float("nan"), device="cuda")
+    mask = torch.full((4, 2, 16), 7, dtype=torch.uint8, device="cuda")
+    m1, b1 = sa.xattn_select_blocks(qd, kd, 1792, True, 0.8, None, chunk=512, workspace=ws,
+                                    block_sum=bs, mask=mask)
+    sa.check_device()
+    assert m1.data_ptr() == mask.data_ptr() and b1.data_ptr() == bs.data_ptr()
+    assert not torch.isnan(bs).any() and torch.all(mask <= 1)
+    m2, b2 = sa.xattn_select_blocks(qd, kd, 1792, True, 0.8, None, chunk=512)
+    sa.check_device()
+    assert torch.equal(b1, b2) and torch.equal(m1, m2)

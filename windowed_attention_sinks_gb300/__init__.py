@@ -75,6 +75,11 @@ def lib() -> ctypes.CDLL:
     L.sattn_xattn_block_sum.restype = ctypes.c_int
     L.sattn_xattn_find_blocks.argtypes = [P, i32, i32, i32, f32, P, P]
     L.sattn_xattn_find_blocks.restype = ctypes.c_int
+    L.sattn_xattn_select_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.sattn_xattn_select_workspace_bytes.restype = sz
+    L.sattn_xattn_select_blocks.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, f32, i32,
+                                            f32, P, sz, P, P, P]
+    L.sattn_xattn_select_blocks.restype = ctypes.c_int
     L.sattn_compress_kv.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, ctypes.c_int,
                                     ctypes.c_int, P]
     L.sattn_compress_kv.restype = ctypes.c_int
@@ -419,24 +424,43 @@ def xattn_find_blocks(block_sum, threshold, mask=None, stream=None):
     return mask
 
 
-def xattn_select_blocks(q, k, q_pos0, causal, threshold, scale=None, chunk=4096, stream=None):
-    """The whole selection as the pages stage it: partial stats per KV chunk,
-    their merge, block sums per chunk with the merged stats, then the
-    threshold selection. Returns (mask uint8 [H, QB, KB], block_sum)."""
+def xattn_select_workspace_bytes(M, H, Nctx, chunk=4096):
+    """Workspace bytes of xattn_select_blocks (sattn_xattn_select_workspace_bytes)."""
+    return int(lib().sattn_xattn_select_workspace_bytes(int(M), int(H), int(Nctx), int(chunk)))
+
+
+def xattn_select_blocks(q, k, q_pos0, causal, threshold, scale=None, chunk=4096, workspace=None,
+                        block_sum=None, mask=None, stream=None):
+    """The whole selection in one call (sattn_xattn_select_blocks): partial
+    stats per KV chunk of `chunk` keys, their merge, block sums with the
+    merged stats, the threshold selection. Returns (mask uint8 [H, QB, KB],
+    block_sum float32 [H, QB, KB])."""
     import torch
 
-    M, H, _ = q.shape
-    Nctx = k.shape[0]
-    chunks = [(a, min(a + chunk, Nctx)) for a in range(0, Nctx, chunk)] or [(0, 0)]
-    mp = torch.empty((len(chunks), M, H), dtype=torch.float32, device=q.device)
-    lp = torch.empty_like(mp)
-    for c, (a, b) in enumerate(chunks):
-        xattn_partial_stats(q, k, q_pos0, a, b, causal, scale, m=mp[c], l=lp[c], stream=stream)
-    m, l = xattn_merge_stats(mp, lp, stream=stream)
-    bs = torch.zeros((H, -(-M // BLOCK), -(-Nctx // BLOCK)), dtype=torch.float32, device=q.device)
-    for a, b in chunks:
-        xattn_block_sum(q, k, m, l, q_pos0, a, b, causal, scale, block_sum=bs, stream=stream)
-    return xattn_find_blocks(bs, threshold, stream=stream), bs
+    M, H, d = q.shape
+    Nctx, Hkv = k.shape[0], k.shape[1]
+    _need(q, "q", torch.bfloat16, q.device)
+    _need(k, "k", torch.bfloat16, q.device)
+    shape = (H, -(-M // BLOCK), -(-Nctx // BLOCK))
+    if block_sum is None:
+        block_sum = torch.empty(shape, dtype=torch.float32, device=q.device)
+    if mask is None:
+        mask = torch.empty(shape, dtype=torch.uint8, device=q.device)
+    _need(block_sum, "block_sum", torch.float32, q.device)
+    _need(mask, "mask", torch.uint8, q.device)
+    if tuple(block_sum.shape) != shape or tuple(mask.shape) != shape:
+        raise ValueError("block_sum and mask must have shape %s" % (shape,))
+    nb = xattn_select_workspace_bytes(M, H, Nctx, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", None, q.device)
+    scale = float(d ** -0.5 if scale is None else scale)
+    _check("sattn_xattn_select_blocks",
+           lib().sattn_xattn_select_blocks(_ptr(q), _ptr(k), M, Nctx, H, Hkv, d, int(q_pos0),
+                                           int(bool(causal)), scale, int(chunk), float(threshold),
+                                           _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _ptr(block_sum), _ptr(mask), _stream(stream)))
+    return mask, block_sum
 
 
 def check_device(stream=None):

@@ -308,7 +308,7 @@ sattn_status sattn_quantize_kv_fp8(const void *kv, uint8_t *kv_nope, void *kv_ro
 static sattn_status xattn_check(const void *q, const void *k, int32_t M, int32_t Nctx, int32_t H,
                                 int32_t Hkv, int32_t d, int32_t q_pos0, int32_t kv_begin,
                                 int32_t kv_end, int32_t causal, float scale) {
-    if (M < 0 || Nctx < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0 || q_pos0 < 0)
+    if (M < 0 || Nctx < 0 || H <= 0 || H > 65535 || Hkv <= 0 || H % Hkv != 0 || q_pos0 < 0)
         return SATTN_ERR_INVALID_ARG;
     if (kv_begin < 0 || kv_end > Nctx || kv_begin > kv_end || (causal != 0 && causal != 1))
         return SATTN_ERR_INVALID_ARG;
@@ -385,6 +385,45 @@ sattn_status sattn_xattn_find_blocks(const float *block_sum, int32_t H, int32_t 
     if (sattn_status st = check_arch(dev)) return st;
     cudaStream_t s = as_stream(cuda_stream);
     return finish(launch_xattn_find_blocks(block_sum, H * QB, KB, threshold, mask, s), s);
+}
+
+size_t sattn_xattn_select_workspace_bytes(int32_t M, int32_t H, int32_t Nctx, int32_t chunk) {
+    if (M <= 0 || H <= 0 || Nctx <= 0 || chunk <= 0) return 0;
+    const size_t C = ((size_t)Nctx + (size_t)chunk - 1) / (size_t)chunk;
+    return (2 * C + 2) * (size_t)M * (size_t)H * sizeof(float);
+}
+
+sattn_status sattn_xattn_select_blocks(const void *q, const void *k, int32_t M, int32_t Nctx,
+                                       int32_t H, int32_t Hkv, int32_t d, int32_t q_pos0,
+                                       int32_t causal, float scale, int32_t chunk,
+                                       float threshold, void *workspace, size_t workspace_bytes,
+                                       float *block_sum, uint8_t *mask, void *cuda_stream) {
+    if (sattn_status st = xattn_check(q, k, M, Nctx, H, Hkv, d, q_pos0, 0, Nctx, causal, scale))
+        return st;
+    if (chunk <= 0 || chunk % 128 != 0 || !(threshold >= 0.f && threshold <= 1.f))
+        return SATTN_ERR_INVALID_ARG;
+    const int64_t C = ((int64_t)Nctx + chunk - 1) / chunk;
+    const int64_t QB = ((int64_t)M + 127) / 128, KB = ((int64_t)Nctx + 127) / 128;
+    if (C > 65535 || KB > 4096 || (int64_t)H * QB > 0x7fffffff) return SATTN_ERR_INVALID_ARG;
+    if (M == 0 || Nctx == 0) return SATTN_OK;
+    if (!workspace || !block_sum || !mask || !aligned16(workspace) ||
+        workspace_bytes < sattn_xattn_select_workspace_bytes(M, H, Nctx, chunk))
+        return SATTN_ERR_INVALID_ARG;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    const int64_t R = (int64_t)M * H;
+    float *mp = static_cast<float *>(workspace), *lp = mp + C * R, *m = lp + C * R, *l = m + R;
+    XattnArgs a1{q, k, M, Nctx, H, Hkv, q_pos0, 0, Nctx, causal, scale, mp, lp, nullptr, chunk};
+    e = launch_xattn_stats(a1, *dev, s);
+    if (e == cudaSuccess) e = launch_xattn_merge_stats(mp, lp, (int)C, R, m, l, s);
+    XattnArgs a3{q, k, M, Nctx, H, Hkv, q_pos0, 0, Nctx, causal, scale, m, l, block_sum, 0};
+    if (e == cudaSuccess) e = launch_xattn_block_sum(a3, *dev, s);
+    if (e == cudaSuccess)
+        e = launch_xattn_find_blocks(block_sum, (int)(H * QB), (int)KB, threshold, mask, s);
+    return finish(e, s);
 }
 
 sattn_status sattn_merge_lse(const float *o_parts, const float *lse_parts, int32_t C, int64_t R,

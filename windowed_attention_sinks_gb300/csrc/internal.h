@@ -106,6 +106,7 @@ struct XattnArgs {
     float scale;
     float *m, *l;      // [M, H]
     float *block_sum;  // [H, ceil(M/128), ceil(Nctx/128)]
+    int chunk;         // stage 1: keys per (m, l) output, outputs [C, M, H]; 0: one output
 };
 
 // SIMT kernels: any dtype, d in {64, 128}.
