@@ -153,3 +153,56 @@ def test_out_of_range_index_is_reported_not_faulted():
     with pytest.raises(sa.SattnError) as e:
         sa.check_device()
     assert e.value.code == 4
+
+
+def _decode_inputs(case):
+    q, kv = dev(case.q, torch.bfloat16), dev(case.kv, torch.bfloat16)
+    idx = dev(case.idx, torch.int32)
+    s = dev(case.sinks, torch.float32)
+    nb = sa.sparse_workspace_bytes(case.B, case.M, case.H, case.d, case.K)
+    return q, kv, idx, s, nb
+
+
+def test_split_merge_reuses_a_workspace_and_ignores_its_contents():
+    # split lists: a workspace full of random bytes, then the same workspace
+    # again and again, all give the oracle's result and the same bits
+    case = W.sparse_decode_bf16(11, B=16)
+    q, kv, idx, s, nb = _decode_inputs(case)
+    ws = torch.randint(0, 256, (nb,), dtype=torch.uint8, device="cuda")
+    ro, rl = oracle_sparse(case)
+    first = None
+    for it in range(4):
+        o, lse = sa.sparse_fwd(q, kv, idx, s, case.sink_mode, case.scale, workspace=ws)
+        sa.check_device()
+        compare(o, lse, ro, rl, TOL_BF16_O, what="reuse %d" % it)
+        if first is None:
+            first = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o, first[0]) and torch.equal(lse, first[1])
+
+
+def test_split_merge_under_graph_replay():
+    # a captured split call (the gathered kernel and the merge) gives the
+    # oracle's result on every replay
+    case = W.sparse_decode_bf16(12, B=32)
+    q, kv, idx, s, nb = _decode_inputs(case)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    o = torch.empty((case.B, case.M, case.H, case.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((case.B, case.M, case.H), dtype=torch.float32, device="cuda")
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        sa.sparse_fwd(q, kv, idx, s, case.sink_mode, case.scale, o=o, lse=lse, workspace=ws,
+                      stream=st)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        sa.sparse_fwd(q, kv, idx, s, case.sink_mode, case.scale, o=o, lse=lse, workspace=ws,
+                      stream=st)
+    ro, rl = oracle_sparse(case)
+    for it in range(3):
+        o.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        sa.check_device()
+        compare(o, lse, ro, rl, TOL_BF16_O, what="replay %d" % it)
