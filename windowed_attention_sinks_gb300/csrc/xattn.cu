@@ -77,13 +77,6 @@ __host__ __device__ constexpr uint32_t koff(int kk) {
     return ((uint32_t)(kk >> 2) * HALF + (uint32_t)(kk & 3) * 32u) >> 4;
 }
 
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *m, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(m)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // One work item: its piece of the key range, [kv_begin, kv_end), the key
 // tiles [kb_lo, kb_hi) that some row of its units may see, and the units.
 struct Item {
