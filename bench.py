@@ -508,24 +508,18 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         units = case.M
         flush = None
 
-        side = torch.cuda.Stream(device=device)
-        ev_go, ev_done = torch.cuda.Event(), torch.cuda.Event()
+        chunk = case.chunks[0][1] - case.chunks[0][0]
 
         def launch(st=None):
-            # the chunks are independent: they alternate between two streams,
-            # so that a chunk's grid fills the SMs the previous one's tail
-            # leaves idle; the merge waits for both
-            ev_go.record(stream)
-            side.wait_event(ev_go)
-            for c, (a, b) in enumerate(case.chunks):
-                sa.block_sparse_fwd(q, k, v, mask, case.q_pos0, a, b, True, case.scale,
-                                    o_part=op[c].view(case.M, case.H, case.d),
-                                    lse_part=lp[c].view(case.M, case.H),
-                                    stream=stream if c % 2 == 0 else side)
-            ev_done.record(side)
-            stream.wait_event(ev_done)
-            sa.merge_lse(op, lp, case.H, o=o, lse=lse, stream=stream)
-        name = "block-sparse bf16: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 chunks + merge"
+            # every chunk in one launch over (chunk, query block, head), then
+            # the LSE merge of the eight partials
+            st = st or stream
+            sa.block_sparse_chunks_fwd(q, k, v, mask, case.q_pos0, 0, case.k.shape[0], chunk, True,
+                                       case.scale, o_parts=op.view(C, case.M, case.H, case.d),
+                                       lse_parts=lp.view(C, case.M, case.H), stream=st)
+            sa.merge_lse(op, lp, case.H, o=o, lse=lse, stream=st)
+        name = ("block-sparse bf16: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 chunks in one "
+                "launch + merge")
 
     for _ in range(args.warmup):
         launch()
@@ -598,7 +592,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                      "tflops": tf,
                      "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
         # sparse: the gathered-attention kernel, plus the merge when lists are split
-        "gpu_launches": args.steps * (len(case.chunks) + 1 if args.workload == "block"
+        "gpu_launches": args.steps * (2 if args.workload == "block"
                                       else 4 if args.workload == "select"
                                       else 2 if args.workload == "index" or nb > 0 else 1),
         "clocks": clk.summary(),

@@ -189,6 +189,26 @@ sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,
                                     float *lse_part, sattn_dtype dtype, void *cuda_stream);
 
 /*
+ * All chunks of a block-sparse call at once: [kv_begin, kv_end) is cut into
+ * C = ceil((kv_end - kv_begin) / chunk) chunks [kv_begin + c chunk,
+ * min(kv_end, kv_begin + (c + 1) chunk)), and chunk c writes o_parts[c]
+ * (float32 [C, M, H, d]) and lse_parts[c] ([C, M, H]) exactly as
+ * sattn_block_sparse_fwd called on that chunk would, bit for bit. With BF16
+ * this is one launch over every (chunk, query block, head); F32 runs one
+ * launch per chunk. Merge with sattn_merge_lse (C, R = M * H).
+ * Requirements: those of sattn_block_sparse_fwd, and chunk > 0
+ * (SATTN_ERR_INVALID_ARG otherwise). M == 0 or kv_begin == kv_end: nothing
+ * to do.
+ */
+sattn_status sattn_block_sparse_chunks_fwd(const void *q, const void *k, const void *v,
+                                           const uint8_t *block_mask, int32_t M, int32_t Nctx,
+                                           int32_t H, int32_t Hkv, int32_t d, int32_t q_pos0,
+                                           int32_t kv_begin, int32_t kv_end, int32_t chunk,
+                                           int32_t causal, float scale, float *o_parts,
+                                           float *lse_parts, sattn_dtype dtype,
+                                           void *cuda_stream);
+
+/*
  * Index lists over a [window ring | compressed] cache ("DeepSeek-V4 CSA/HCA
  * walkthrough", section 2.3 steps 5-6: the window indices concatenated with
  * the compressed-region indices form topk_idxs; section 3.3: cache layout

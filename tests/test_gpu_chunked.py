@@ -116,3 +116,33 @@ def test_merge_kernel(C, with_sinks):
     ro, rl = oracle.merge(op.astype(np.float32).astype(np.float64),
                           lp.astype(np.float32).astype(np.float64), H, sinks)
     compare(o, lse, ro, rl, 1e-5, what="merge C=%d" % C)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("Nctx,M,chunk,kv_begin,kv_end", [(2048, 512, 512, 0, 2048),
+                                                          (2300, 300, 1000, 0, 2300),
+                                                          (4096, 256, 768, 640, 3900),
+                                                          (1024, 128, 4096, 0, 1024)])
+def test_all_chunks_in_one_call_match_the_chunk_calls(dt, Nctx, M, chunk, kv_begin, kv_end):
+    # every chunk at once (one launch over (chunk, query block, head) with
+    # bf16) gives each chunk's partials bit for bit; chunks need not be
+    # aligned to key blocks, and the last one may be short
+    case = W.block_sparse_bf16(5, Nctx=Nctx, M=M, chunk=chunk, density=0.3)
+    q, k, v = dev(case.q, dt), dev(case.k, dt), dev(case.v, dt)
+    mask = dev(case.mask, torch.uint8)
+    o_all, l_all = sa.block_sparse_chunks_fwd(q, k, v, mask, case.q_pos0, kv_begin, kv_end, chunk,
+                                              True, case.scale)
+    sa.check_device()
+    bounds = [(a, min(a + chunk, kv_end)) for a in range(kv_begin, kv_end, chunk)]
+    assert o_all.shape[0] == len(bounds)
+    for c, (a, b) in enumerate(bounds):
+        o1, l1 = sa.block_sparse_fwd(q, k, v, mask, case.q_pos0, a, b, True, case.scale)
+        sa.check_device()
+        assert torch.equal(o_all[c], o1) and torch.equal(l_all[c], l1), c
+    # and the merge of the chunk partials against the oracle over the range
+    o, lse = sa.merge_lse(o_all.reshape(len(bounds), M * case.H, case.d),
+                          l_all.reshape(len(bounds), M * case.H), case.H, out_dtype=dt)
+    ro, rl = oracle.block_sparse(case.q, case.k, case.v, case.mask, case.q_pos0, kv_begin, kv_end,
+                                 1, case.scale)
+    compare(o.reshape(M, case.H, case.d), lse.reshape(M, case.H), ro, rl,
+            TOL_BF16_O if dt == torch.bfloat16 else TOL_F32_O, what="merged chunks")

@@ -56,6 +56,9 @@ def lib() -> ctypes.CDLL:
     L.sattn_block_sparse_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                          f32, P, P, ctypes.c_int, P]
     L.sattn_block_sparse_fwd.restype = ctypes.c_int
+    L.sattn_block_sparse_chunks_fwd.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                i32, i32, i32, f32, P, P, ctypes.c_int, P]
+    L.sattn_block_sparse_chunks_fwd.restype = ctypes.c_int
     L.sattn_build_topk_idxs.argtypes = [P, P, i32, i32, i32, i32, i32, P]
     L.sattn_build_topk_idxs.restype = ctypes.c_int
     L.sattn_kv_ring_write.argtypes = [P, P, P, i32, i32, i32, i32, i32, ctypes.c_int, P]
@@ -278,6 +281,33 @@ def block_sparse_fwd(q, k, v, block_mask, q_pos0, kv_begin, kv_end, causal=True,
                                         _dtype_code(q), _stream(stream))
     _check("sattn_block_sparse_fwd", code)
     return o_part, lse_part
+
+
+def block_sparse_chunks_fwd(q, k, v, block_mask, q_pos0, kv_begin, kv_end, chunk, causal=True,
+                            scale=None, o_parts=None, lse_parts=None, stream=None):
+    """Every chunk of `chunk` keys of [kv_begin, kv_end) at once
+    (sattn_block_sparse_chunks_fwd): fp32 partials [C, M, H, d] and [C, M, H],
+    the same as block_sparse_fwd chunk by chunk."""
+    import torch
+
+    M, H, d = q.shape
+    Nctx, Hkv = k.shape[0], k.shape[1]
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, q.dtype, q.device)
+    _need(block_mask, "block_mask", torch.uint8, q.device)
+    C = -(-(int(kv_end) - int(kv_begin)) // int(chunk)) if chunk > 0 else 0
+    if o_parts is None:
+        o_parts = torch.empty((C, M, H, d), dtype=torch.float32, device=q.device)
+    if lse_parts is None:
+        lse_parts = torch.empty((C, M, H), dtype=torch.float32, device=q.device)
+    scale = float(d ** -0.5 if scale is None else scale)
+    code = lib().sattn_block_sparse_chunks_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_mask), M,
+                                               Nctx, H, Hkv, d, int(q_pos0), int(kv_begin),
+                                               int(kv_end), int(chunk), int(bool(causal)), scale,
+                                               _ptr(o_parts), _ptr(lse_parts), _dtype_code(q),
+                                               _stream(stream))
+    _check("sattn_block_sparse_chunks_fwd", code)
+    return o_parts, lse_parts
 
 
 def build_topk_idxs(start_pos, M, K, win, ratio, out=None, stream=None):

@@ -10,6 +10,8 @@
 #include <new>
 
 #include "common.cuh"
+#include <algorithm>
+
 #include "internal.h"
 
 namespace sattn {
@@ -527,6 +529,48 @@ sattn_status sattn_block_sparse_fwd(const void *q, const void *k, const void *v,
         return finish(launch_block_tc(a, *dev, s), s);
     }
     return finish(launch_block_simt(a, *dev, s), s);
+}
+
+sattn_status sattn_block_sparse_chunks_fwd(const void *q, const void *k, const void *v,
+                                           const uint8_t *block_mask, int32_t M, int32_t Nctx,
+                                           int32_t H, int32_t Hkv, int32_t d, int32_t q_pos0,
+                                           int32_t kv_begin, int32_t kv_end, int32_t chunk,
+                                           int32_t causal, float scale, float *o_parts,
+                                           float *lse_parts, sattn_dtype dtype,
+                                           void *cuda_stream) {
+    if (M < 0 || Nctx < 0 || H <= 0 || Hkv <= 0 || H % Hkv != 0) return SATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return SATTN_ERR_INVALID_ARG;
+    if (q_pos0 < 0 || kv_begin < 0 || kv_end > Nctx || kv_begin > kv_end || chunk <= 0)
+        return SATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return SATTN_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype) || !finite_scale(scale)) return SATTN_ERR_INVALID_ARG;
+    const int64_t C = ((int64_t)kv_end - kv_begin + chunk - 1) / chunk;
+    if (M == 0 || C == 0) return SATTN_OK;
+    if (!q || !o_parts || !lse_parts || !k || !v || !block_mask) return SATTN_ERR_INVALID_ARG;
+    if (dtype == SATTN_BF16 && d != 128) return SATTN_ERR_UNSUPPORTED;
+    cudaError_t e;
+    const DevInfo *dev = device_info(&e);
+    if (!dev) return SATTN_ERR_CUDA;
+    if (sattn_status st = check_arch(dev)) return st;
+    cudaStream_t s = as_stream(cuda_stream);
+    if (dtype == SATTN_BF16) {
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_parts))
+            return SATTN_ERR_INVALID_ARG;
+        BlockArgs a{q, k, v, block_mask, M, Nctx, H, Hkv, d, q_pos0, kv_begin, kv_end, causal,
+                    scale, o_parts, lse_parts, (int)dtype, chunk};
+        return finish(launch_block_tc(a, *dev, s), s);
+    }
+    // F32: one launch per chunk
+    const size_t rows = (size_t)M * H;
+    for (int64_t c = 0; c < C; ++c) {
+        const int b0 = kv_begin + (int)(c * chunk);
+        const int b1 = (int)std::min<int64_t>(kv_end, (int64_t)b0 + chunk);
+        BlockArgs a{q, k, v, block_mask, M, Nctx, H, Hkv, d, q_pos0, b0, b1, causal, scale,
+                    o_parts + (size_t)c * rows * d, lse_parts + (size_t)c * rows, (int)dtype, 0};
+        e = launch_block_simt(a, *dev, s);
+        if (e != cudaSuccess) break;
+    }
+    return finish(e, s);
 }
 
 }  // extern "C"

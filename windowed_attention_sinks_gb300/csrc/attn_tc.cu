@@ -83,7 +83,8 @@ struct TcParams {
     // block
     const uint8_t *mask;
     int M, Nctx, q_pos0, kv_begin, kv_end, QB, KB;
-    float *o_part, *lse_part;
+    int chunk_keys;        // [kv_begin, kv_end) in chunks of this many keys, one output each
+    float *o_part, *lse_part;  // [chunk, M, H, d] and [chunk, M, H]
     unsigned *work;  // zeroed per launch: next item to claim
 };
 
@@ -94,7 +95,8 @@ struct Item {
     int q_row0;    // first row of the tile in q / o (token index)
     int key_row0;  // global K/V row of key coordinate 0
     int qpos0;     // window: local index of query row 0; block: absolute position
-    int lo, hi, L; // window: key band of the tile (local), sequence length
+    int lo, hi, L; // window: key band of the tile (local), sequence length;
+                   // block: the chunk's keys [lo, hi) and the chunk's index
     const uint8_t *mrow;
     int kb_lo, kb_hi, kend;  // block: 128-key block range, key limit
     float sink;              // window: the head's sink (0 when there is none)
@@ -167,17 +169,20 @@ template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &
         it.sink = p.sinks ? __ldg(p.sinks + it.h) : 0.f;
         it.valid = true;
     } else {
-        const int qb = rest;
+        const int qb = rest % p.QB;
+        it.L = rest / p.QB;  // chunk
+        it.lo = p.kv_begin + it.L * p.chunk_keys;
+        it.hi = (int)min((long long)p.kv_end, (long long)it.lo + p.chunk_keys);
         const int qs = qb * BM;
         it.nq = min(BM, p.M - qs);
         it.q_row0 = qs;
         it.key_row0 = 0;
         it.qpos0 = p.q_pos0 + qs;
-        int end = p.kv_end;
+        int end = it.hi;
         if (p.causal) end = min(end, it.qpos0 + it.nq);
         it.kend = end;
-        it.kb_lo = p.kv_begin / 128;
-        it.kb_hi = end > p.kv_begin ? (end - 1) / 128 : it.kb_lo - 1;
+        it.kb_lo = it.lo / 128;
+        it.kb_hi = end > it.lo ? (end - 1) / 128 : it.kb_lo - 1;
         it.mrow = p.mask + ((size_t)it.h * p.QB + qb) * p.KB;
         int n = 0;
         for (int kb = it.kb_lo; kb <= it.kb_hi; ++kb) {
@@ -185,7 +190,7 @@ template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &
             // 64-key halves that overlap [kv_begin, end)
             for (int hh = 0; hh < 2; ++hh) {
                 const int base = kb * 128 + hh * BN;
-                n += (base < end && base + BN > p.kv_begin) ? 1 : 0;
+                n += (base < end && base + BN > it.lo) ? 1 : 0;
             }
         }
         it.ntiles = n;
@@ -209,7 +214,7 @@ template <int MODE> struct TileIter {
                 hh = 1;
             }
             const int base = kb * 128 + hh * BN;
-            if (base < it.kend && base + BN > p.kv_begin) {
+            if (base < it.kend && base + BN > it.lo) {
                 ++j;
                 return base;
             }
@@ -435,13 +440,16 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
         bool valid;
         int q_row0, nq, h;
         float m, l;
+        size_t row_off;  // block: the chunk's first output row
     };
     Pend pend{false, 0, 0, 0, 0.f, 0.f};
     auto epilogue = [&](const Pend &pe) -> bool {
         if (!mbar_wait(smem_u32(&b.o_full), qi & 1, ctx, abort)) return false;
         tc_fence_after();
         const float inv = pe.l > 0.0f ? 1.0f / pe.l : 0.0f;
-        const size_t orow = (size_t)(pe.q_row0 + r) * p.H + pe.h;
+        // block: the chunk's rows; window: no offset (folded at compile time)
+        const size_t roff = MODE == MODE_BLOCK ? pe.row_off : 0;
+        const size_t orow = roff + (size_t)(pe.q_row0 + r) * p.H + pe.h;
         // Each pass covers 128 bytes of every row: this thread's row goes to
         // the warp's staging buffer (128B-swizzled, conflict-free), then the
         // warp writes 4 whole rows (4 lines) per store instruction.
@@ -493,7 +501,7 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
                                  : "r"(sb + (uint32_t)rw * 128u + (((uint32_t)unit ^ ((uint32_t)rw & 7u)) << 4)));
                     const int rr = quarter * 32 + rw;
                     if (rr < pe.nq) {
-                        const size_t grow = (size_t)(pe.q_row0 + rr) * p.H + pe.h;
+                        const size_t grow = roff + (size_t)(pe.q_row0 + rr) * p.H + pe.h;
                         *reinterpret_cast<uint4 *>(obase + grow * ROW_BYTES + pass * 128 + unit * 16) = v;
                     }
                 }
@@ -524,7 +532,7 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
         const bool row_valid = r < it.nq;
         if (it.ntiles == 0) {  // block mode: nothing visible in this chunk
             if (MODE == MODE_BLOCK && row_valid) {
-                const size_t orow = (size_t)(it.q_row0 + r) * p.H + it.h;
+                const size_t orow = (size_t)it.L * p.M * p.H + (size_t)(it.q_row0 + r) * p.H + it.h;
                 float4 *dst = reinterpret_cast<float4 *>(p.o_part + orow * HD);
 #pragma unroll 8
                 for (int i = 0; i < HD / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -560,8 +568,8 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
             const int base = ti.next(p, it);
             if (MODE == MODE_BLOCK) {
                 if (row_valid) {
-                    lo_r = max(base, p.kv_begin);
-                    hi_r = min(base + BN - 1, p.kv_end - 1);
+                    lo_r = max(base, it.lo);
+                    hi_r = min(base + BN - 1, it.hi - 1);
                     if (p.causal) hi_r = min(hi_r, qi_loc);
                 } else {
                     lo_r = NONE_LO;
@@ -682,7 +690,8 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
             }
         }
         if (!ok) break;
-        pend = Pend{true, it.q_row0, it.nq, it.h, m_run, l};
+        pend = Pend{true, it.q_row0, it.nq, it.h, m_run, l,
+                    MODE == MODE_BLOCK ? (size_t)it.L * p.M * p.H : 0};
     }
     if (ok && pend.valid) epilogue(pend);
 }
@@ -848,7 +857,11 @@ cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t
     p.KB = (a.Nctx + 127) / 128;
     p.o_part = a.o_part;
     p.lse_part = a.lse_part;
-    const long long items = (long long)p.QB * a.H;
+    // chunk 0 (or a chunk as long as the range): one output for the range
+    const int len = a.kv_end - a.kv_begin;
+    p.chunk_keys = a.chunk > 0 && a.chunk < len ? a.chunk : len;
+    const long long chunks = (len + p.chunk_keys - 1) / p.chunk_keys;
+    const long long items = (long long)p.QB * a.H * chunks;
     if (items > INT_MAX) return cudaErrorInvalidValue;
     p.num_items = (int)items;
     if (reinterpret_cast<uintptr_t>(a.o_part) & 15u) return cudaErrorMisalignedAddress;

@@ -73,8 +73,9 @@ struct BlockArgs {
     const uint8_t *mask;
     int M, Nctx, H, Hkv, d, q_pos0, kv_begin, kv_end, causal;
     float scale;
-    float *o_part, *lse_part;
+    float *o_part, *lse_part;  // [C, M, H, d], [C, M, H]
     int dtype;
+    int chunk;  // > 0: [kv_begin, kv_end) in C chunks of this many keys; 0: one chunk
 };
 
 struct MergeArgs {
