@@ -144,6 +144,18 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert lib.sattn_xattn_find_blocks(fake, 2, 2, 4, f32(1.5), fake, None) == 1
     assert lib.sattn_xattn_find_blocks(fake, 2, 2, 5000, f32(0.9), fake, None) == 1
     assert lib.sattn_xattn_merge_stats(None, None, 0, 0, None, None, None) == 0
+    # all chunks at once: chunk <= 0, range past Nctx, H % Hkv; an empty
+    # range or no rows is no work
+    assert lib.sattn_block_sparse_chunks_fwd(fake, fake, fake, fake, 128, 1024, 4, 2, 128, 0, 0,
+                                             1024, 0, 1, f32(0.1), fake, fake, 1, None) == 1
+    assert lib.sattn_block_sparse_chunks_fwd(fake, fake, fake, fake, 128, 1024, 4, 2, 128, 0, 0,
+                                             2048, 256, 1, f32(0.1), fake, fake, 1, None) == 1
+    assert lib.sattn_block_sparse_chunks_fwd(fake, fake, fake, fake, 128, 1024, 4, 3, 128, 0, 0,
+                                             1024, 256, 1, f32(0.1), fake, fake, 1, None) == 1
+    assert lib.sattn_block_sparse_chunks_fwd(None, None, None, None, 128, 1024, 4, 2, 128, 0, 512,
+                                             512, 256, 1, f32(0.1), None, None, 1, None) == 0
+    assert lib.sattn_block_sparse_chunks_fwd(None, None, None, None, 0, 1024, 4, 2, 128, 0, 0,
+                                             1024, 256, 1, f32(0.1), None, None, 1, None) == 0
     # the one-call selection: chunk not a multiple of 128 or 0, threshold out
     # of range, workspace too small or misaligned, too many key blocks, more
     # heads than a grid dimension holds; no rows is no work

@@ -154,7 +154,7 @@ sattn_status check_arch(const DevInfo *dev) {
 
 extern "C" {
 
-int32_t sattn_version(void) { return 102; }
+int32_t sattn_version(void) { return 103; }
 
 const char *sattn_status_str(sattn_status s) {
     switch (s) {
