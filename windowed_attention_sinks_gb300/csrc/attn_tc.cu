@@ -375,11 +375,15 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
         const int n = it.ntiles, kt0 = kt;
         auto issue_pv = [&](int jj) -> bool {
             const int st = (kt0 + jj) % VSTAGES, use = (kt0 + jj) / VSTAGES;
-            if (!mbar_wait(smem_u32(&b.p_full[pc & 1]), (pc >> 1) & 1, ctx, abort)) return false;
+            // the stage and O waits first, P (written by the softmax, the one
+            // this thread usually waits for) last: each barrier access of this
+            // thread stalls the MMAs in flight, so the last one should be the
+            // one that releases the issue
             if (!mbar_wait(smem_u32(&b.v_full[st]), use & 1, ctx, abort)) return false;
             if (jj == 0 && qi >= 1 &&
                 !mbar_wait(smem_u32(&b.o_empty), (qi - 1) & 1, ctx, abort))
                 return false;
+            if (!mbar_wait(smem_u32(&b.p_full[pc & 1]), (pc >> 1) & 1, ctx, abort)) return false;
             tc_fence_after();
             const uint64_t dv = st ? dv1 : dv0;
             const uint32_t p_tmem = tmem + P_COL + 32u * (uint32_t)(pc & 1);
@@ -396,8 +400,9 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
         for (int j = 0; ok && j < n; ++j) {
             // one S buffer: tile t may start once the softmax has loaded tile t-1
             const int t = kt0 + j, st = t % KSTAGES, use = t / KSTAGES;
-            if (t >= 1) ok = mbar_wait(smem_u32(&b.s_empty), (t - 1) & 1, ctx, abort);
-            if (ok) ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort);
+            // the key stage first, the softmax's release of S last (as above)
+            ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort);
+            if (ok && t >= 1) ok = mbar_wait(smem_u32(&b.s_empty), (t - 1) & 1, ctx, abort);
             if (!ok) break;
             tc_fence_after();
             const uint64_t dk = st ? dk1 : dk0;
