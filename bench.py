@@ -106,6 +106,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# the ncu record behind each workload's roofline.traffic: (kernel, source file);
+# bytes per unit of the workload (query, or compressed row)
+TRAFFIC_RECORD = {
+    "decode": ("sparse_tc_kernel<decode>", "sparse_tc.cu"),
+    "prefill": ("sparse_tc_kernel<prefill>", "sparse_tc.cu"),
+    "decode_fp8": ("sparse_tc_kernel<decode_fp8>", "sparse_tc.cu"),
+    "prefill_fp8": ("sparse_tc_kernel<prefill_fp8>", "sparse_tc.cu"),
+    "block": ("attn_tc_kernel<block>", "attn_tc.cu"),
+    "select": ("xattn_tc_kernel<1>", "xattn.cu"),
+    "compress": ("compress_kernel", "compress.cu"),
+}
+
+
 def profiled_traffic(kernel, source_name, units):
     """DRAM bytes per launch from the committed ncu record, scaled to `units`
     query tokens; None when the kernel source changed since the capture."""
@@ -585,9 +598,8 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                    else "inputs larger than L2",
                    "launch": "CUDA graph replay" if graph is not None else "direct"},
         "roofline": {**roof,
-                     "traffic": profiled_traffic("sparse_tc_kernel<%s>" % args.workload,
-                                                 "sparse_tc.cu", units)
-                     if args.workload in ("decode", "prefill") else None,
+                     "traffic": profiled_traffic(*TRAFFIC_RECORD[args.workload], units)
+                     if args.workload in TRAFFIC_RECORD else None,
                      "peak_source": peaks_src,
                      "tflops": tf,
                      "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
