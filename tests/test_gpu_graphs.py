@@ -81,3 +81,41 @@ def test_selection_under_graph_replay():
         sa.xattn_select_blocks(q, k, Nctx - M, True, 0.9, None, chunk=1024, workspace=ws,
                                block_sum=bs, mask=mask, stream=st)
     _replays_match(call, [bs, mask])
+
+
+def test_window_calls_on_two_streams_at_once():
+    # two different problems in flight together, each launch with its own
+    # work counter: the results equal those of the calls made one at a time
+    cases = [W.window_vision_bf16(5, 16, num_seqs=48), W.window_vision_bf16(6, 8, num_seqs=40)]
+    ins, outs = [], []
+    for case in cases:
+        q, k, v = (dev(x, torch.bfloat16) for x in (case.q, case.k, case.v))
+        cu = dev(case.cu_seqlens, torch.int32)
+        s = dev(case.sinks, torch.float32)
+        ins.append((case, q, k, v, cu, s))
+        T = case.q.shape[0]
+        outs.append((torch.empty((T, case.H, case.d), dtype=torch.bfloat16, device="cuda"),
+                     torch.empty((T, case.H), dtype=torch.float32, device="cuda")))
+
+    def run(i, st):
+        case, q, k, v, cu, s = ins[i]
+        o, lse = outs[i]
+        sa.window_fwd(q, k, v, cu, case.max_seqlen, case.window_left, case.window_right,
+                      case.causal, s, sa.SINK_KEY0_BIAS, case.scale, o=o, lse=lse, stream=st)
+    st = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for i in range(2):
+        run(i, st[i])
+        st[i].synchronize()
+    sa.check_device()
+    want = [(o.clone(), lse.clone()) for o, lse in outs]
+    for rep in range(3):
+        for o, lse in outs:
+            o.zero_()
+            lse.zero_()
+        torch.cuda.synchronize()
+        for i in range(2):
+            run(i, st[i])
+        torch.cuda.synchronize()
+        sa.check_device()
+        for (o, lse), (wo, wl) in zip(outs, want):
+            assert torch.equal(o, wo) and torch.equal(lse, wl), rep
