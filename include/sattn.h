@@ -4,8 +4,21 @@
  * C ABI of libsattn.so. Every tensor argument is a DEVICE pointer to a
  * contiguous, row-major buffer unless stated otherwise; scalars are passed by
  * value. The caller owns every buffer; the library allocates no device or
- * host memory and keeps no state beyond a per-device cache of attributes,
- * tensor-map entry points and the address of its device error word.
+ * host memory. Its state: on the host, a per-device cache of attributes and
+ * device addresses, the tensor-map encoder entry point, the debug flag and
+ * wait limit, and a launch counter; on each device, module-scope arrays built
+ * into the library: the error word, a ring of 256 item-claim words and the
+ * scratch array of sattn_sparse_fwd_static_scratch.
+ *
+ * Claim words: each launch of the window and block-sparse kernels takes the
+ * next word of the ring (zeroed on its stream) and tags it with a per-launch
+ * number; its CTAs claim work items from it. A launch that finds the word
+ * tagged by another launch (two launches 256 apart in issue order that
+ * overlap on the GPU, e.g. on different streams or in concurrently replayed
+ * CUDA graphs) never modifies it and takes its remaining items in a static
+ * order instead: results stay exact, only the load balance suffers. Replaying
+ * ONE captured graph concurrently with itself is not supported (it also
+ * writes the same output buffers).
  *
  * Execution: every compute call is asynchronous on `cuda_stream` (a
  * cudaStream_t; NULL selects the per-thread default stream, never the legacy
@@ -133,8 +146,10 @@ size_t sattn_sparse_workspace_bytes(int32_t B, int32_t M, int32_t H, int32_t d, 
  * partial results of a split index list go to a fixed array of
  * SATTN_SPARSE_STATIC_SCRATCH_BYTES compiled into the library, which every GPU
  * that loads the library holds until the process exits. Nothing is allocated.
- * A call whose sattn_sparse_workspace_bytes(B, M, H, d, K) exceeds that size
- * is rejected with SATTN_ERR_INVALID_ARG before anything runs.
+ * Only bf16 calls with H = 32 and d = 128 can split lists and use the array;
+ * such a call whose sattn_sparse_workspace_bytes(B, M, H, d, K) exceeds its
+ * size is rejected with SATTN_ERR_INVALID_ARG before anything runs. Other
+ * shapes never need it and are not limited by it.
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture. All calls share the array and it keeps the last call's contents
@@ -315,7 +330,7 @@ sattn_status sattn_sparse_fp8_fwd(const void *q, const uint8_t *kv_nope, const v
  *   block_sum float32 [H, QB, KB].
  * Step 4, sattn_xattn_find_blocks: for each (h, qb) the key blocks ordered by
  *   block_sum (largest first, the lower kb first among equal values; negative
- *   values count as 0) and the shortest leading run whose cumulative sum
+ *   and NaN values count as 0) and the shortest leading run whose cumulative sum
  *   (float64, in that order) reaches threshold x their total is selected:
  *   mask[h, qb, kb] = 1 (uint8 [H, QB, KB]), others 0; nothing where the total
  *   is 0. Requirements: 0 <= threshold <= 1, KB <= 4096.

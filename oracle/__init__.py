@@ -428,14 +428,17 @@ def xattn_find_blocks(block_sum, threshold):
     (largest first, the lower block first among equal masses) and the
     shortest leading run of them whose cumulative mass reaches threshold x
     the total is selected. Sums in float64, in that order, from the given
-    values (a kernel's fp32 sums reproduce the decisions exactly). Returns
-    uint8 [H, QB, KB]; nothing is selected where the total is not positive."""
+    values (a kernel's fp32 sums reproduce the decisions exactly). A block
+    mass is a sum of probabilities, so it cannot be negative; a given value
+    that is negative or NaN counts as a mass of 0 (the library's contract for
+    caller-supplied sums). Returns uint8 [H, QB, KB]; nothing is selected
+    where the total is not positive."""
     bs = np.asarray(block_sum)
     H, QB, KB = bs.shape
     out = np.zeros((H, QB, KB), dtype=np.uint8)
     for h in range(H):
         for qb in range(QB):
-            v = [float(x) for x in bs[h, qb]]
+            v = [float(x) if float(x) > 0.0 else 0.0 for x in bs[h, qb]]
             order = sorted(range(KB), key=lambda kb: (-v[kb], kb))
             total = 0.0
             for kb in order:

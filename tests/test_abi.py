@@ -187,3 +187,10 @@ def test_workspace_size_monotone(lib):
     big = lib.sattn_sparse_workspace_bytes(64, 1, 32, 128, 640)
     assert big >= small >= 0
     assert lib.sattn_sparse_workspace_bytes(0, 1, 32, 128, 640) == 0
+
+
+def test_workspace_bytes_for_huge_batches(lib):
+    # B * M beyond 32 bits needs no split (and must not overflow or divide by zero)
+    assert lib.sattn_sparse_workspace_bytes(65536, 65536, 32, 128, 640) == 0
+    assert lib.sattn_sparse_workspace_bytes(2 ** 31 - 1, 2, 32, 128, 640) == 0
+    assert lib.sattn_sparse_workspace_bytes(2 ** 31 - 1, 2 ** 31 - 1, 32, 128, 640) == 0

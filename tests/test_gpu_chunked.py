@@ -154,3 +154,68 @@ def test_all_chunks_in_one_call_match_the_chunk_calls(dt, Nctx, M, chunk, kv_beg
                                  1, case.scale)
     compare(o.reshape(M, case.H, case.d), lse.reshape(M, case.H), ro, rl,
             TOL_BF16_O if dt == torch.bfloat16 else TOL_F32_O, what="merged chunks")
+
+
+def _support_counts(o, lse):
+    """With q = 0 every visible key has the same weight: lse = ln|S| and
+    o = (counts of the one-hot codes of the visible keys) / |S|. Rounding
+    recovers |S| and the integer counts exactly (fp32 partials)."""
+    lse = np.asarray(lse, dtype=np.float64)
+    n = np.rint(np.exp(lse))  # -inf (nothing visible) -> 0
+    counts = np.rint(np.asarray(o, dtype=np.float64) * n[..., None])
+    return n.astype(np.int64), counts.astype(np.int64)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_block_mask_decisions_bit_exact(dt):
+    """Visible sets of the block-sparse path, bit for bit: q = 0 and one-hot
+    values, first v_j = e_(j mod 128) (the key's offset in its block), then
+    v_j = e_(j // 128) (its block). Per row and chunk, |S| and both code
+    histograms must equal the oracle's exactly. Chunk bounds and q_pos0 are
+    not multiples of 128, so the chunk edges cut blocks, the causal limit
+    cuts the diagonal blocks, and the mask is random elsewhere."""
+    rng = np.random.default_rng(21)
+    M, Nctx, H, Hkv, d = 300, 2600, 4, 2, 128
+    q_pos0, kv_begin, kv_end, chunk = 2250, 77, 2555, 700
+    QB, KB = -(-M // 128), -(-Nctx // 128)
+    mask = (rng.random((H, QB, KB)) < 0.45).astype(np.uint8)
+    for qb in range(QB):  # blocks on the causal diagonal of each query block
+        lo, hi = (q_pos0 + 128 * qb) // 128, (q_pos0 + min(M, 128 * qb + 128) - 1) // 128
+        mask[:, qb, lo:hi + 1] = 1
+    mask[1, 0, :] = 0  # a (head, query block) that sees nothing
+    q = np.zeros((M, H, d), np.float32)
+    k = W.round_bf16(rng.standard_normal((Nctx, Hkv, d)).astype(np.float32))
+    bounds = [(a, min(a + chunk, kv_end)) for a in range(kv_begin, kv_end, chunk)]
+    j = np.arange(Nctx)
+    for code in (j % 128, j // 128):
+        v = np.zeros((Nctx, Hkv, d), np.float32)
+        v[j, :, code] = 1.0
+        case = W.BlockSparseCase(q=q, k=k, v=v, mask=mask, q_pos0=q_pos0, chunk=chunk,
+                                 scale=d ** -0.5, dtype="bf16" if dt == torch.bfloat16 else "f32")
+        qd, kd, vd, md = dev(q, dt), dev(k, dt), dev(v, dt), dev(mask, torch.uint8)
+        o_all, l_all = sa.block_sparse_chunks_fwd(qd, kd, vd, md, q_pos0, kv_begin, kv_end, chunk,
+                                                  True, case.scale)
+        sa.check_device()
+        refs = []
+        for c, (a, b) in enumerate(bounds):
+            ro, rl = oracle.block_sparse(q, k, v, mask, q_pos0, a, b, 1, case.scale)
+            refs.append((ro, rl))
+            n_ref, h_ref = _support_counts(ro, rl)
+            o1, l1 = sa.block_sparse_fwd(qd, kd, vd, md, q_pos0, a, b, True, case.scale)
+            sa.check_device()
+            for what, (og, lg) in (("one chunk", (o1, l1)), ("all chunks", (o_all[c], l_all[c]))):
+                n_got, h_got = _support_counts(og.cpu().numpy(), lg.cpu().numpy())
+                assert np.array_equal(n_got, n_ref), "%s %d: |S| differs" % (what, c)
+                assert np.array_equal(h_got, h_ref), "%s %d: visible keys differ" % (what, c)
+        # the partials merged over [kv_begin, kv_end) against the one-shot oracle
+        C = len(bounds)
+        o, lse = sa.merge_lse(o_all.reshape(C, M * H, d), l_all.reshape(C, M * H), H,
+                              out_dtype=torch.float32)
+        ro, rl = oracle.block_sparse(q, k, v, mask, q_pos0, kv_begin, kv_end, 1, case.scale)
+        n_ref, h_ref = _support_counts(ro, rl)
+        n_got, h_got = _support_counts(o.reshape(M, H, d).cpu().numpy(),
+                                       lse.reshape(M, H).cpu().numpy())
+        assert np.array_equal(n_got, n_ref) and np.array_equal(h_got, h_ref), "merged"
+        # the case exercises what it claims: empty rows, rows cut by the
+        # chunk edges, and rows whose diagonal block is partly visible
+        assert (n_ref == 0).any() and (n_ref > 0).any()

@@ -187,3 +187,45 @@ def test_one_call_reuses_caller_buffers():
     m2, b2 = sa.xattn_select_blocks(qd, kd, 1792, True, 0.8, None, chunk=512)
     sa.check_device()
     assert torch.equal(b1, b2) and torch.equal(m1, m2)
+
+
+def test_find_blocks_counts_negative_and_nan_sums_as_zero():
+    # caller-supplied sums may hold values a probability mass cannot take;
+    # the kernel and the oracle both count negatives, -0 and NaN as 0
+    rng = np.random.default_rng(11)
+    H, QB, KB = 3, 5, 37
+    bs = rng.random((H, QB, KB)).astype(np.float32)
+    neg = rng.random((H, QB, KB)) < 0.3
+    bs[neg] = -rng.random(int(neg.sum())).astype(np.float32) * 2
+    bs[0, 0, :] = -1.0            # a row with nothing positive: nothing selected
+    bs[0, 1, 3] = np.float32(-0.0)
+    bs[0, 1, 4] = np.nan
+    bs[1, 2, :5] = [0.4, -3.0, 0.4, np.nan, 0.2]
+    for thr in (0.0, 0.5, 0.9, 1.0):
+        mask = sa.xattn_find_blocks(torch.from_numpy(bs).cuda(), thr)
+        sa.check_device()
+        want = oracle.xattn_find_blocks(bs, thr)
+        assert np.array_equal(mask.cpu().numpy(), want), thr
+        assert not want[0, 0].any()
+
+
+def test_selection_flips_against_fp64_block_sums():
+    # the kernel's fp32 block sums against the oracle's fp64 ones: thresholding
+    # is discontinuous, so a block whose cumulative mass sits at the threshold
+    # may flip; count how many decisions differ end to end
+    case = W.block_sparse_bf16(0, Nctx=4096, M=1024, chunk=1024)
+    q, k = case.q, case.k
+    scale = case.scale
+    mask, bs = sa.xattn_select_blocks(dev(q, torch.bfloat16), dev(k, torch.bfloat16), case.q_pos0,
+                                      True, 0.9, scale, chunk=1024)
+    sa.check_device()
+    wm, wl = oracle.xattn_partial_stats(q, k, case.q_pos0, 0, case.Nctx, True, scale)
+    want_bs = oracle.xattn_block_sum(q, k, wm, wl, case.q_pos0, 0, case.Nctx, True, scale)
+    want = oracle.xattn_find_blocks(want_bs, 0.9)
+    got = mask.cpu().numpy()
+    flips = int((got != want).sum())
+    # stage by stage the decisions are exact (the oracle on the kernel's sums)
+    assert np.array_equal(got, oracle.xattn_find_blocks(bs.cpu().numpy(), 0.9))
+    print("selection decisions that differ from the fp64 chain: %d of %d (%d selected)" % (
+        flips, got.size, int(want.sum())))
+    assert flips <= max(2, got.size // 200)

@@ -124,6 +124,11 @@ def test_a_dominant_key_takes_its_block():
     ([0.1, 0.0, 0.9], 1.0, [1, 0, 1]),    # zero mass never needed
     ([0.1, 0.0, 0.9], 0.0, [0, 0, 1]),    # the first block always
     ([0.0, 0.0, 0.0], 0.9, [0, 0, 0]),    # nothing to select
+    # a mass is never negative: given negative or NaN sums count as 0
+    ([0.5, -1.0, 0.3], 0.9, [1, 0, 1]),   # total 0.8, not -0.2
+    ([-0.5, -0.1, 0.0], 0.5, [0, 0, 0]),  # total 0: nothing
+    ([float("nan"), 0.4, 0.6], 1.0, [0, 1, 1]),
+    ([-0.0, 0.3, -2.0], 1.0, [0, 1, 0]),
 ])
 def test_selection_by_hand(sums, thr, want):
     got = oracle.xattn_find_blocks(np.array([[sums]]), thr)

@@ -15,10 +15,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import windowed_attention_sinks_gb300 as sa
 from windowed_attention_sinks_gb300 import workloads as W
 
-from gpu_helpers import TOL_BF16_O, compare, dev
+from gpu_helpers import TOL_BF16_O, TOL_F32_O, compare, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -68,12 +69,41 @@ def test_static_scratch_matches_workspace_entry_point():
         ref_l = lse_ref.float().cpu().numpy().reshape(-1).astype(np.float64)
         compare(o.reshape(-1, case.d), lse.reshape(-1), ref_o, ref_l, TOL_BF16_O,
                 what="static scratch, call %d" % seed)
+        # and against the oracle itself
+        ro, rl = oracle.sparse(case.q, case.kv, case.idx, case.sinks, case.sink_mode, case.scale)
+        compare(o, lse, ro, rl, TOL_BF16_O, what="static scratch vs oracle, call %d" % seed)
+
+
+def test_static_scratch_takes_shapes_that_need_no_scratch():
+    # fp32 runs on the SIMT path, which never splits lists: a shape whose
+    # tensor-core split would need more than the built-in array is accepted
+    B, M, H, d, N, K = 64, 1, 64, 128, 300, 4096
+    assert sa.sparse_workspace_bytes(B, M, H, d, K) > STATIC_SCRATCH_BYTES
+    rng = np.random.default_rng(5)
+    case = W.SparseCase(q=rng.standard_normal((B, M, H, d)).astype(np.float32),
+                        kv=rng.standard_normal((B, N, d)).astype(np.float32),
+                        idx=rng.integers(-1, N, size=(B, M, K)).astype(np.int32),
+                        sinks=rng.standard_normal(H).astype(np.float32), scale=d ** -0.5,
+                        sink_mode=2, dtype="f32")
+    q, kv = dev(case.q, torch.float32), dev(case.kv, torch.float32)
+    idx, sinks = dev(case.idx, torch.int32), dev(case.sinks, torch.float32)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, M, H), dtype=torch.float32, device="cuda")
+    rc = _entry()(q.data_ptr(), kv.data_ptr(), idx.data_ptr(), sinks.data_ptr(), 2, case.scale,
+                  o.data_ptr(), lse.data_ptr(), B, M, H, d, N, K, sa.F32,
+                  torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, rc
+    sa.check_device()
+    rows = np.arange(0, B * M * H, 37)
+    ro, rl = oracle.sparse(case.q, case.kv, case.idx, case.sinks, 2, case.scale, rows=rows)
+    sel = torch.from_numpy(rows).cuda()
+    compare(o.reshape(-1, d)[sel], lse.reshape(-1)[sel], ro, rl, TOL_F32_O, what="fp32 static")
 
 
 def test_static_scratch_refuses_oversized_requests():
-    # 128 single-token requests of 64 heads x 256 with long lists, split in two,
-    # need about 17 MB of partials
-    B, M, H, d, N, K = 128, 1, 64, 256, 16, 4096
+    # 64 single-token requests (32 heads, d = 128) with 4096-entry lists, split
+    # eight ways on the tensor-core path, need about 8.5 MB of partials
+    B, M, H, d, N, K = 64, 1, 32, 128, 16, 4096
     assert sa.sparse_workspace_bytes(B, M, H, d, K) > STATIC_SCRATCH_BYTES
     rng = np.random.default_rng(0)
     case = W.SparseCase(q=W.round_bf16(rng.standard_normal((B, M, H, d)).astype(np.float32)),

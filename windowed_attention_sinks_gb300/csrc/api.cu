@@ -17,10 +17,10 @@
 namespace sattn {
 
 __device__ unsigned g_error_word;
-// Per-launch counters of the persistent kernels (claimed items, arrivals of
-// split partials): a ring of blocks, each cleared on the launch's stream.
-constexpr unsigned kCounterBlocks = 64;
-__device__ unsigned g_counters[kCounterBlocks * kCounterBlock];
+// Item-claim words of the persistent kernels, one per launch in turn, each on
+// its own 128-byte line.
+constexpr unsigned kClaimStride = 16;
+__device__ unsigned long long g_claims[kClaimWords * kClaimStride];
 
 namespace {
 
@@ -79,8 +79,8 @@ const DevInfo *device_info(cudaError_t *e) {
         void *p = nullptr;
         if ((*e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return nullptr;
         d.err = static_cast<unsigned *>(p);
-        if ((*e = cudaGetSymbolAddress(&p, g_counters)) != cudaSuccess) return nullptr;
-        d.counters = static_cast<unsigned *>(p);
+        if ((*e = cudaGetSymbolAddress(&p, g_claims)) != cudaSuccess) return nullptr;
+        d.claims = static_cast<unsigned long long *>(p);
         if ((*e = cudaMemset(d.err, 0, sizeof(unsigned))) != cudaSuccess) return nullptr;
         if ((*e = cudaDeviceSynchronize()) != cudaSuccess) return nullptr;
         g_dev[dev] = d;
@@ -91,15 +91,34 @@ const DevInfo *device_info(cudaError_t *e) {
 
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
-unsigned *launch_counters(const DevInfo &dev, cudaStream_t s, unsigned n, cudaError_t *e) {
-    if (n == 0 || n > kCounterBlock) {
-        *e = cudaErrorInvalidValue;
-        return nullptr;
-    }
+unsigned long long *launch_claim_word(const DevInfo &dev, cudaStream_t s, unsigned *tag,
+                                      cudaError_t *e) {
     static std::atomic<unsigned> next{0};
-    unsigned *c = dev.counters + (size_t)(next.fetch_add(1) % kCounterBlocks) * kCounterBlock;
-    *e = cudaMemsetAsync(c, 0, n * sizeof(unsigned), s);
-    return *e == cudaSuccess ? c : nullptr;
+    const unsigned n = next.fetch_add(1);
+    *tag = n % 0xffffffffu + 1u;  // never 0: a zero word is free
+    unsigned long long *w = dev.claims + (size_t)(n % kClaimWords) * kClaimStride;
+    *e = cudaMemsetAsync(w, 0, sizeof(*w), s);
+    return *e == cudaSuccess ? w : nullptr;
+}
+
+cudaError_t ensure_smem_attr(const void *kernel, size_t bytes, const DevInfo &dev) {
+    struct Entry {
+        const void *fn;
+        int device;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int ndone = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ndone; ++i)
+        if (done[i].fn == kernel && done[i].device == dev.device && done[i].bytes >= bytes)
+            return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    if (ndone < 256) done[ndone++] = Entry{kernel, dev.device, bytes};
+    return cudaSuccess;
 }
 
 bool verbose() {

@@ -15,20 +15,32 @@ struct DevInfo {
     int device = -1;
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
-    unsigned *err = nullptr;       // device address of the error word
-    unsigned *counters = nullptr;  // device address of the per-launch counter blocks
+    unsigned *err = nullptr;                 // device address of the error word
+    unsigned long long *claims = nullptr;    // device address of the claim-word ring
 };
 
 // Per-device facts, initialised once per device (thread-safe).
 const DevInfo *device_info(cudaError_t *e);
 uint64_t wait_limit_ns();
-// n (<= kCounterBlock) zeroed counters for one launch on `s`: the next block
-// of a ring of 64 built into the library, cleared by an asynchronous memset
-// on `s`. A block is reused 64 launches later, so launches on different
-// streams do not share counters unless 64 of them overlap. Returns nullptr
-// (and sets *e) if n is out of range or the memset cannot be issued.
-constexpr unsigned kCounterBlock = 512;
-unsigned *launch_counters(const DevInfo &dev, cudaStream_t s, unsigned n, cudaError_t *e);
+
+// The item-claim word of one launch of a persistent kernel that hands out
+// work items dynamically. The word holds (tag << 32 | items claimed); the
+// launch's tag is unique among the last 2^32 - 1 launches. The word is the
+// next of a ring of kClaimWords built into the library and is zeroed by an
+// asynchronous memset on `s`. A kernel claims by compare-and-swap and never
+// modifies a word that carries another launch's tag (zero counts as free);
+// when it finds one, because an overlapping launch reused the ring entry, it
+// switches to a static schedule of the remaining items. Overlapping launches
+// therefore never lose or repeat each other's items; sharing an entry only
+// costs the dynamic balancing. Returns nullptr (and sets *e) if the memset
+// cannot be issued.
+constexpr unsigned kClaimWords = 256;
+unsigned long long *launch_claim_word(const DevInfo &dev, cudaStream_t s, unsigned *tag,
+                                      cudaError_t *e);
+
+// cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per
+// (kernel, device, size), thread-safe.
+cudaError_t ensure_smem_attr(const void *kernel, size_t bytes, const DevInfo &dev);
 // True when the environment variable SATTN_VERBOSE is set (launch reports on stderr).
 bool verbose();
 

@@ -57,7 +57,10 @@ extern "C" sattn_status sattn_sparse_fwd_static_scratch(
     const void *q, const void *kv_cache, const int32_t *topk_idxs, const float *sinks,
     sattn_sink_mode sink_mode, float scale, void *o, float *lse, int32_t B, int32_t M, int32_t H,
     int32_t d, int32_t N, int32_t K, sattn_dtype dtype, void *cuda_stream) {
-    const size_t need = sattn_sparse_workspace_bytes(B, M, H, d, K);
+    // only the tensor-core path (bf16, 32 heads, d = 128) splits lists and
+    // uses the scratch; the other shapes run without it
+    const bool uses_scratch = dtype == SATTN_BF16 && H == 32 && d == 128;
+    const size_t need = uses_scratch ? sattn_sparse_workspace_bytes(B, M, H, d, K) : 0;
     if (need > (size_t)SATTN_SPARSE_STATIC_SCRATCH_BYTES) {
         if (sattn::verbose())
             fprintf(stderr,

@@ -947,11 +947,11 @@ sparse_tc_kernel(const __grid_constant__ CUtensorMap tq, const SpParams p, const
 }
 
 int choose_splits(int B, int M, int K, int sm_count) {
-    const int items = B * M;
+    const long long items = (long long)B * M;
     const int max_split = (K + R - 1) / R;
     // two items run per SM; aim for one round of items
-    if (max_split <= 1 || items >= NSLOT * sm_count) return 1;
-    int s = (NSLOT * sm_count) / items;
+    if (max_split <= 1 || items <= 0 || items >= (long long)NSLOT * sm_count) return 1;
+    int s = (int)((NSLOT * sm_count) / items);
     if (s > max_split) s = max_split;
     if (s > MAX_SPLITS) s = MAX_SPLITS;
     return s < 1 ? 1 : s;
@@ -1022,12 +1022,9 @@ cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream
     }
     const size_t smem = sizeof(Smem);
     auto kernel = fp8 ? sparse_tc_kernel<true> : sparse_tc_kernel<false>;
-    static bool attr_set[2][64] = {};
-    if (!attr_set[fp8][dev.device & 63]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        cudaError_t e = ensure_smem_attr((const void *)kernel, smem, dev);
         if (e != cudaSuccess) return e;
-        attr_set[fp8][dev.device & 63] = true;
     }
     DevCtx ctx{dev.err, wait_limit_ns()};
     if (verbose())

@@ -482,8 +482,8 @@ __global__ void merge_stats_kernel(const float *__restrict__ m_parts,
 
 // Step 4: one CTA per (head, query block). The key blocks are sorted by
 // (mass descending, block ascending) with a bitonic sort of 64-bit keys in
-// shared memory (masses are >= 0, so their bit patterns order like the
-// values); one thread then walks them in that order with float64 sums.
+// shared memory (masses are taken as >= 0, so their bit patterns order like
+// the values); one thread then walks them in that order with float64 sums.
 constexpr int FB_THREADS = 256;
 constexpr int FB_MAX = 4096;  // key blocks per row supported
 
@@ -499,7 +499,8 @@ find_blocks_kernel(const float *__restrict__ block_sum, int KB, float threshold,
     for (int i = threadIdx.x; i < n; i += FB_THREADS) {
         unsigned long long key = ~0ull;  // padding sorts last
         if (i < KB) {
-            const float x = fmaxf(v[i], 0.f);
+            // a negative, -0 or NaN mass counts as +0 (whose bits sort last)
+            const float x = v[i] > 0.f ? v[i] : 0.f;
             key = ((unsigned long long)(0xffffffffu - __float_as_uint(x)) << 32) | (unsigned)i;
         }
         keys[i] = key;
@@ -591,12 +592,9 @@ cudaError_t launch_tc(const XattnArgs &a, const DevInfo &dev, cudaStream_t s) {
         make_map(&tk, a.k, a.Nctx > 0 ? a.Nctx : 1, a.Hkv) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
-    static bool attr_set[64] = {};
-    if (!attr_set[dev.device & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(xattn_tc_kernel<MODE>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        cudaError_t e = ensure_smem_attr((const void *)xattn_tc_kernel<MODE>, smem, dev);
         if (e != cudaSuccess) return e;
-        attr_set[dev.device & 63] = true;
     }
     DevCtx ctx{dev.err, wait_limit_ns()};
     const int grid = (int)std::min<long long>(items, dev.sm_count > 0 ? dev.sm_count : 1);
