@@ -196,11 +196,9 @@ def test_block_mask_decisions_bit_exact(dt):
         o_all, l_all = sa.block_sparse_chunks_fwd(qd, kd, vd, md, q_pos0, kv_begin, kv_end, chunk,
                                                   True, case.scale)
         sa.check_device()
-        refs = []
         for c, (a, b) in enumerate(bounds):
             ro, rl = oracle.block_sparse(q, k, v, mask, q_pos0, a, b, 1, case.scale)
-            refs.append((ro, rl))
-            n_ref, h_ref = _support_counts(ro, rl)
+            n_ref, h_ref = _support_counts(ro.reshape(M, H, d), rl.reshape(M, H))
             o1, l1 = sa.block_sparse_fwd(qd, kd, vd, md, q_pos0, a, b, True, case.scale)
             sa.check_device()
             for what, (og, lg) in (("one chunk", (o1, l1)), ("all chunks", (o_all[c], l_all[c]))):
@@ -212,7 +210,7 @@ def test_block_mask_decisions_bit_exact(dt):
         o, lse = sa.merge_lse(o_all.reshape(C, M * H, d), l_all.reshape(C, M * H), H,
                               out_dtype=torch.float32)
         ro, rl = oracle.block_sparse(q, k, v, mask, q_pos0, kv_begin, kv_end, 1, case.scale)
-        n_ref, h_ref = _support_counts(ro, rl)
+        n_ref, h_ref = _support_counts(ro.reshape(M, H, d), rl.reshape(M, H))
         n_got, h_got = _support_counts(o.reshape(M, H, d).cpu().numpy(),
                                        lse.reshape(M, H).cpu().numpy())
         assert np.array_equal(n_got, n_ref) and np.array_equal(h_got, h_ref), "merged"
