@@ -234,18 +234,23 @@ def run_sattn(args, rank, world, device):
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(total_q, world, ms_per_step)
     # Roofline of the dominant launch (Hkv = 16: the most bytes per launch),
-    # averaged over its key-0 and null-logit launches.
+    # the median over its key-0 and null-logit launches; beside it every
+    # launch's own figure and the whole step's (all four launches' bytes over
+    # the sum of their median times).
     lm = np.array(launch_ms)  # [steps, launches]
+    med = np.median(lm, axis=0)
     dom = [i for i, (c, _, _, _, _) in enumerate(launches) if c.Hkv == max(x[0].Hkv for x in launches)]
-    dom_ms = float(np.mean(lm[:, dom]))
+    dom_ms = float(np.median(lm[:, dom]))
     dom_bytes, dom_flops = launches[dom[0]][3], launches[dom[0]][4]
     achieved_gbs = dom_bytes / (dom_ms / 1e3) / 1e9
     achieved_tf = dom_flops / (dom_ms / 1e3) / 1e12
     peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     traffic = profiled_traffic("attn_tc_kernel<window>", "attn_tc.cu", launches[dom[0]][0].T)
     variants = [{"hkv": c.Hkv, "sink_mode": "key0_bias" if m == 1 else "null_logit",
-                 "ms": float(np.mean(lm[:, i])), "gbs": b / (float(np.mean(lm[:, i])) / 1e3) / 1e9}
+                 "ms": float(med[i]), "gbs": b / (float(med[i]) / 1e3) / 1e9,
+                 "frac": b / (float(med[i]) / 1e3) / 1e9 / peak}
                 for i, (c, m, _, b, _) in enumerate(launches)]
+    step_gbs = total_bytes / (float(med.sum()) / 1e3) / 1e9
     out = {
         "metric": "queries/s (window attention, bf16, 256 varlen seqs, H=16, Hkv 16+8, "
                   "d=128, w=128, key0_bias+null_logit)",
@@ -266,12 +271,22 @@ def run_sattn(args, rank, world, device):
                      "launch_ms": dom_ms, "algorithmic_bytes": dom_bytes,
                      "avg_launch_ms_all": avg_launch_ms, "tflops": achieved_tf,
                      "tensor_frac": achieved_tf / peaks.get("bf16_tflops_sustained", 1700.0),
-                     "variants": variants},
+                     "variants": variants,
+                     "whole_step": {"achieved": step_gbs, "frac": step_gbs / peak,
+                                    "bytes": int(total_bytes), "ms": float(med.sum())},
+                     "timing": "median of %d steps per launch" % args.steps},
         "gpu_launches": len(launches) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.no_e2e:
         out["e2e"] = e2e_window(args, launches, device, stream)
+    if not args.no_paths:
+        # the other paths of the hot path, each timed in this run (median of 50)
+        for t in dev_inputs.values():
+            t.clear()
+        torch.cuda.empty_cache()
+        out["paths"] = measure_paths(["decode", "prefill", "block"], rank, world, device, peaks,
+                                     peaks_src)
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline_window(launches)
     return out
@@ -381,20 +396,27 @@ def cpu_baseline_window(launches, budget_s=15.0):
                       "pass, fp64, %.1f s" % (seqs, done_q, spent)}
 
 
-def run_other(args, rank, world, device, peaks, peaks_src):
-    """Decode / prefill / block-sparse measurement lines (same JSON shape)."""
+class Path:
+    """One measured path: a launch function over device-resident inputs and
+    its algorithmic work per step."""
+
+    def __init__(self, **kw):
+        self.__dict__.update(kw)
+
+
+def build_path(workload, seed, device, stream):
+    """Inputs and launch function of a non-window workload (decode | prefill |
+    decode_fp8 | prefill_fp8 | block | select | index | compress)."""
     import torch
 
     import windowed_attention_sinks_gb300 as sa
     from windowed_attention_sinks_gb300 import workloads as W
 
-    stream = torch.cuda.current_stream()
     bf = torch.bfloat16
-    seed = rank_seed(rank)
-    if args.workload in ("decode", "prefill", "decode_fp8", "prefill_fp8"):
-        fp8 = args.workload.endswith("_fp8")
-        case = W.sparse_decode_bf16(seed) if args.workload.startswith("decode") else \
-            W.sparse_prefill_bf16(seed)
+    if workload in ("decode", "prefill", "decode_fp8", "prefill_fp8"):
+        fp8 = workload.endswith("_fp8")
+        decode = workload.startswith("decode")
+        case = W.sparse_decode_bf16(seed) if decode else W.sparse_prefill_bf16(seed)
         q = torch.from_numpy(case.q).to(bf).to(device)
         kv = torch.from_numpy(case.kv).to(bf).to(device)
         idx = torch.from_numpy(case.idx).to(device)
@@ -408,11 +430,6 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         # d bytes of RoPE part + a 4-byte scale
         row_bytes = (case.d // 2 + case.d + 4) if fp8 else case.d * 2
         nbytes = valid * row_bytes + case.idx.size * 4 + 2 * q.numel() * 2 + lse.numel() * 4
-        flops = 4 * case.d * valid * case.H
-        units = case.B * case.M
-        # decode is tiny: a scratch buffer larger than L2 is rewritten before every launch
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device) \
-            if args.workload.startswith("decode") else None
         if fp8:
             kv_nope, kv_rope, kv_scale = sa.quantize_kv_fp8(kv, case.d // 2)
             del kv
@@ -424,34 +441,47 @@ def run_other(args, rank, world, device, peaks, peaks_src):
             else:
                 sa.sparse_fwd(q, kv, idx, sinks, case.sink_mode, case.scale, o=o, lse=lse,
                               workspace=ws, stream=st or stream)
-        name = "sparse %s %s: B=%d M=%d H=%d d=%d N=%d K=%d null_logit" % (
-            args.workload.replace("_fp8", ""),
-            "bf16 q, FP8 cache (e4m3 + row scale, bf16 RoPE half)" if fp8 else "bf16",
-            case.B, case.M, case.H, case.d, case.N, case.K)
-    elif args.workload == "index":
+        # launches per step: the cluster kernel alone for bf16 decode (its
+        # splits merge on chip), else the persistent kernel plus the merge
+        # when it splits lists
+        if decode and not fp8:
+            kernel, launches = "sparse_decode_kernel", 1
+        else:
+            kernel = "sparse_tc_kernel<%s>" % workload
+            launches = 2 if decode else 1
+        return Path(
+            launch=launch, units=case.B * case.M, nbytes=nbytes,
+            flops=4 * case.d * valid * case.H,
+            # decode is tiny: a scratch buffer larger than L2 is rewritten before each step
+            flush=decode, graph=decode, launches=launches, kernel=kernel,
+            bound="tensor" if not decode else "hbm",
+            traffic_key=None if (decode and not fp8) else workload,
+            name="sparse %s %s: B=%d M=%d H=%d d=%d N=%d K=%d null_logit" % (
+                workload.replace("_fp8", ""),
+                "bf16 q, FP8 cache (e4m3 + row scale, bf16 RoPE half)" if fp8 else "bf16",
+                case.B, case.M, case.H, case.d, case.N, case.K))
+    if workload == "index":
         # cache bookkeeping of the prefill layout: index lists of 8192 queries
         # (K = 2048, window 128, ratio 4) and the ring write of the prompt's KV
-        nb = 0
         M, K, win, ratio, d = 8192, 2048, 128, 4, 128
         starts = torch.zeros(1, dtype=torch.int32, device=device)
         idx_out = torch.empty((1, M, K), dtype=torch.int32, device=device)
         cache = torch.zeros((1, win + 8192, d), dtype=bf, device=device)
         new_kv = torch.randn((1, M, d), device=device).to(bf)
-        nbytes = idx_out.numel() * 4 + 2 * win * d * 2
-        flops = 0
-        units = M
-        # the 67 MB of lists fit in L2: a larger scratch is rewritten before each step
-        flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
 
         def launch(st=None):
             sa.build_topk_idxs(starts, M, K, win, ratio, out=idx_out, stream=st or stream)
             sa.kv_ring_write(cache, new_kv, starts, win, stream=st or stream)
-        name = "cache bookkeeping: topk index lists (8192 queries, K=2048, win 128, ratio 4) + ring write"
-    elif args.workload == "select":
+        # the 67 MB of lists fit in L2: a larger scratch is rewritten before each step
+        return Path(launch=launch, units=M, nbytes=idx_out.numel() * 4 + 2 * win * d * 2,
+                    flops=0, flush=True, graph=True, launches=2, kernel="topk_idxs_kernel",
+                    bound="hbm", traffic_key=None,
+                    name="cache bookkeeping: topk index lists (8192 queries, K=2048, win 128, "
+                         "ratio 4) + ring write")
+    if workload == "select":
         # block selection over the chunked block-sparse workload's shape: the
         # last 4096 positions of a 32768-token context, H=32 over 8 KV heads,
         # eight 4096-key chunks (stats, merge, block sums, threshold 0.9)
-        nb = 0
         case = W.block_sparse_bf16(seed)
         q = torch.from_numpy(case.q).to(bf).to(device)
         k = torch.from_numpy(case.k).to(bf).to(device)
@@ -464,22 +494,20 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         sel = torch.empty(bs.shape, dtype=torch.uint8, device=device)
         # visible (row, key) pairs of all heads; each costs one exponential per pass
         pairs = H * sum(min(Nctx, case.q_pos0 + i + 1) for i in range(M))
-        nbytes = 0
-        flops = 2 * 2 * d * pairs  # QK^T of both passes over the visible pairs
-        units = M
-        flush = None
 
         def launch(st=None):
             # stats of all chunks, merge, block sums, threshold 0.9: four launches
             sa.xattn_select_blocks(q, k, case.q_pos0, True, 0.9, case.scale, chunk=chunk,
                                    workspace=ws, block_sum=bs, mask=sel, stream=st or stream)
-        name = ("block selection: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 x 4096-key "
-                "chunks, threshold 0.9, one call")
-    elif args.workload == "compress":
+        return Path(launch=launch, units=M, nbytes=0, flops=2 * 2 * d * pairs, pairs=pairs,
+                    flush=False, graph=False, launches=4, kernel="xattn_tc_kernel",
+                    bound="tensor", traffic_key="select",
+                    name="block selection: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, "
+                         "8 x 4096-key chunks, threshold 0.9, one call")
+    if workload == "compress":
         # compressor gated pooling: eight 32K-token prefills at ratio 4 with
         # overlapping windows, fp32 projections in, bf16 rows into the
         # compressed region of each request's cache
-        nb = 0
         case = W.compress_case(seed)
         B, S, Wd = case.kv.shape
         d, ratio, win = case.d, case.ratio, 128
@@ -489,126 +517,188 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         ape = torch.from_numpy(case.ape).to(device)
         cache = torch.zeros((B, win + nwin, d), dtype=bf, device=device)
         rows = cache[:, win:]
+
+        def launch(st=None):
+            sa.compress_kv(kvp, scp, ape, ratio, case.overlap, out=rows, stream=st or stream)
         # every projection element read once (the last window's first half is
         # never needed), each row written once
         nbytes = (B * (nwin * ratio * d * (2 if case.overlap else 1)
                        - (ratio * d if case.overlap else 0)) * 2 * 4 + B * nwin * d * 2)
-        flops = 0
-        units = B * nwin
-        flush = None
+        return Path(launch=launch, units=B * nwin, nbytes=nbytes, flops=0, flush=False,
+                    graph=False, launches=1, kernel="compress_kernel", bound="hbm",
+                    traffic_key="compress",
+                    name="compressor gated pooling: B=%d S=%d d=%d ratio=%d overlap, fp32 in, "
+                         "bf16 rows" % (B, S, d, ratio))
+    # block: the chunked block-sparse workload
+    case = W.block_sparse_bf16(seed)
+    q = torch.from_numpy(case.q).to(bf).to(device)
+    k = torch.from_numpy(case.k).to(bf).to(device)
+    v = torch.from_numpy(case.v).to(bf).to(device)
+    mask = torch.from_numpy(case.mask).to(device)
+    C = len(case.chunks)
+    op = torch.empty((C, case.M * case.H, case.d), dtype=torch.float32, device=device)
+    lp = torch.empty((C, case.M * case.H), dtype=torch.float32, device=device)
+    o = torch.empty((case.M * case.H, case.d), dtype=bf, device=device)
+    lse = torch.empty((case.M * case.H,), dtype=torch.float32, device=device)
+    nblk = int(case.mask.sum())
+    nbytes = (q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + 2 * op.numel() * 4
+              + 2 * lp.numel() * 4 + o.numel() * 2 + lse.numel() * 4)
+    chunk = case.chunks[0][1] - case.chunks[0][0]
 
-        def launch(st=None):
-            sa.compress_kv(kvp, scp, ape, ratio, case.overlap, out=rows, stream=st or stream)
-        name = "compressor gated pooling: B=%d S=%d d=%d ratio=%d overlap, fp32 in, bf16 rows" % (
-            B, S, d, ratio)
-    else:
-        nb = 0
-        case = W.block_sparse_bf16(seed)
-        q = torch.from_numpy(case.q).to(bf).to(device)
-        k = torch.from_numpy(case.k).to(bf).to(device)
-        v = torch.from_numpy(case.v).to(bf).to(device)
-        mask = torch.from_numpy(case.mask).to(device)
-        C = len(case.chunks)
-        op = torch.empty((C, case.M * case.H, case.d), dtype=torch.float32, device=device)
-        lp = torch.empty((C, case.M * case.H), dtype=torch.float32, device=device)
-        o = torch.empty((case.M * case.H, case.d), dtype=bf, device=device)
-        lse = torch.empty((case.M * case.H,), dtype=torch.float32, device=device)
-        nblk = int(case.mask.sum())
-        nbytes = (q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + 2 * op.numel() * 4
-                  + 2 * lp.numel() * 4 + o.numel() * 2 + lse.numel() * 4)
-        # causal pairs inside kept blocks (diagonal blocks are half visible)
-        flops = 4 * case.d * (nblk * 128 * 128 - case.H * (case.M // 128) * (128 * 127 // 2))
-        units = case.M
-        flush = None
+    def launch(st=None):
+        # every chunk in one launch over (chunk, query block, head), then
+        # the LSE merge of the eight partials
+        st = st or stream
+        sa.block_sparse_chunks_fwd(q, k, v, mask, case.q_pos0, 0, case.k.shape[0], chunk, True,
+                                   case.scale, o_parts=op.view(C, case.M, case.H, case.d),
+                                   lse_parts=lp.view(C, case.M, case.H), stream=st)
+        sa.merge_lse(op, lp, case.H, o=o, lse=lse, stream=st)
+    # causal pairs inside kept blocks (diagonal blocks are half visible)
+    flops = 4 * case.d * (nblk * 128 * 128 - case.H * (case.M // 128) * (128 * 127 // 2))
+    return Path(launch=launch, units=case.M, nbytes=nbytes, flops=flops, flush=False,
+                graph=False, launches=2, kernel="attn_tc_kernel<block>", bound="hbm",
+                traffic_key="block",
+                name="block-sparse bf16: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 chunks "
+                     "in one launch + merge")
 
-        chunk = case.chunks[0][1] - case.chunks[0][0]
 
-        def launch(st=None):
-            # every chunk in one launch over (chunk, query block, head), then
-            # the LSE merge of the eight partials
-            st = st or stream
-            sa.block_sparse_chunks_fwd(q, k, v, mask, case.q_pos0, 0, case.k.shape[0], chunk, True,
-                                       case.scale, o_parts=op.view(C, case.M, case.H, case.d),
-                                       lse_parts=lp.view(C, case.M, case.H), stream=st)
-            sa.merge_lse(op, lp, case.H, o=o, lse=lse, stream=st)
-        name = ("block-sparse bf16: ctx 32768, 4096 queries, H=32, Hkv=8, d=128, 8 chunks in one "
-                "launch + merge")
+def time_path(p, steps, warmup, stream, world=1, clk=None):
+    """Per-step device times (ms) of a path, each step bracketed by CUDA events
+    on the launch stream: `cold` with L2 flushed (p.flush) or inputs larger
+    than L2, and `warm`, the same steps back to back without a flush."""
+    import torch
 
-    for _ in range(args.warmup):
-        launch()
+    import windowed_attention_sinks_gb300 as sa
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=stream.device) if p.flush else None
+    for _ in range(warmup):
+        p.launch()
     sa.check_device(stream)
     graph = None
-    if args.workload in ("decode", "decode_fp8", "index"):
+    if p.graph:
         # a step of ~10-30 us of device work is replayed from a CUDA graph so
         # that host-side enqueue time stays out of the timed region
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            launch(torch.cuda.current_stream())
+            p.launch(torch.cuda.current_stream())
         graph.replay()
         torch.cuda.synchronize()
         sa.check_device(stream)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(gpu_index(device)) as clk:
-        for s in range(args.steps):
-            if flush is not None:
+
+    def run(n, flushed):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        barrier(world)
+        torch.cuda.synchronize()
+        for s in range(n):
+            if flushed and flush is not None:
                 flush.fill_(s & 0xff)
             evs[s][0].record(stream)
             if graph is not None:
                 graph.replay()
             else:
-                launch()
+                p.launch()
             evs[s][1].record(stream)
         torch.cuda.synchronize()
-    barrier(world)
-    times = [a.elapsed_time(b) for a, b in evs]
-    ms = max_over_ranks(float(np.mean(times)), world)
+        barrier(world)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    if clk is not None:
+        with clk:
+            cold = run(steps, True)
+    else:
+        cold = run(steps, True)
+    warm = run(max(steps, 20), False)
     sa.check_device(stream)
-    gbs = nbytes / (ms / 1e3) / 1e9
-    tf = flops / (ms / 1e3) / 1e12
-    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    roof = {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak}
-    if args.workload == "select":
-        # S = Q K^T of both passes over the visible (row, key) pairs against
-        # the measured bf16 tensor peak, the tighter of the two bounds; beside
-        # it the exponential unit: one MUFU ex2 per visible pair and pass, 32
-        # per clock per SM on this part at the SM clock sampled during the run
-        clk_mhz = clk.summary().get("sm_mhz") or 2070.0
-        ex2_peak = 32 * torch.cuda.get_device_properties(device).multi_processor_count * \
-            clk_mhz * 1e6 / 1e12
-        ex2 = 2 * pairs / (ms / 1e3) / 1e12
-        tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    return cold, warm, graph is not None
+
+
+def path_record(p, cold, warm, peaks, peaks_src, world, clk_mhz=None, sm_count=152):
+    """Median step time, its roofline and the labelled warm-L2 figure."""
+    ms = max_over_ranks(float(np.median(cold)), world)
+    ms_warm = max_over_ranks(float(np.median(warm)), world)
+    gbs = p.nbytes / (ms / 1e3) / 1e9
+    tf = p.flops / (ms / 1e3) / 1e12
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tpeak = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    if p.bound == "tensor":
         roof = {"bound": "tensor", "achieved": tf, "peak": tpeak, "unit": "TFLOP/s",
-                "frac": tf / tpeak,
-                "ex2": {"achieved": ex2, "peak": ex2_peak, "unit": "Tex2/s",
-                        "frac": ex2 / ex2_peak}}
+                "frac": tf / tpeak}
+        if p.nbytes:
+            # the gathered-bytes convention beside it (the cache may live in L2)
+            roof["gathered_bytes"] = {"achieved": gbs, "peak": hbm, "unit": "GB/s",
+                                      "frac": gbs / hbm}
+        if getattr(p, "pairs", None):
+            # one MUFU ex2 per visible pair and pass, 32 per clock per SM
+            ex2_peak = 32 * sm_count * (clk_mhz or 2070.0) * 1e6 / 1e12
+            ex2 = 2 * p.pairs / (ms / 1e3) / 1e12
+            roof["ex2"] = {"achieved": ex2, "peak": ex2_peak, "unit": "Tex2/s",
+                           "frac": ex2 / ex2_peak}
+    else:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                "frac": gbs / hbm}
+    roof["traffic"] = (profiled_traffic(*TRAFFIC_RECORD[p.traffic_key], p.units)
+                       if p.traffic_key in TRAFFIC_RECORD else None)
+    roof["peak_source"] = peaks_src
+    roof["tflops"] = tf
+    roof["tensor_frac"] = tf / peaks.get("bf16_tflops_sustained", 1700.0)
+    return {"ms": ms, "ms_mean": float(np.mean(cold)), "runs": len(cold),
+            "value": whole_job_rate(p.units, world, ms), "unit": "queries/s",
+            "warm_l2_ms": ms_warm, "launches_per_step": p.launches, "kernel": p.kernel,
+            "roofline": roof}
+
+
+def run_other(args, rank, world, device, peaks, peaks_src):
+    """Decode / prefill / block-sparse / ... measurement lines (same JSON shape)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    p = build_path(args.workload, rank_seed(rank), device, stream)
+    clk = ClockSampler(gpu_index(device))
+    cold, warm, graphed = time_path(p, args.steps, args.warmup, stream, world, clk)
+    summ = clk.summary()
+    rec = path_record(p, cold, warm, peaks, peaks_src, world, summ.get("sm_mhz"),
+                      torch.cuda.get_device_properties(device).multi_processor_count)
     unit_name = "compressed rows" if args.workload == "compress" else "queries"
     return {
         "metric": "%s/s (%s)" % (unit_name, args.workload),
-        "value": whole_job_rate(units, world, ms),
+        "value": rec["value"],
         "unit": "%s/s" % unit_name, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": rec["ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if args.workload == "compress" else "bf16",
         "data": "synthetic (seeded numpy PCG64%s)" % (
             ", fp32 projections" if args.workload == "compress" else ", bf16"),
-        "config": {"workload": name,
-                   "l2": "scratch > L2 rewritten before each step" if flush is not None
+        "config": {"workload": p.name,
+                   "l2": "scratch > L2 rewritten before each step" if p.flush
                    else "inputs larger than L2",
-                   "launch": "CUDA graph replay" if graph is not None else "direct"},
-        "roofline": {**roof,
-                     "traffic": profiled_traffic(*TRAFFIC_RECORD[args.workload], units)
-                     if args.workload in TRAFFIC_RECORD else None,
-                     "peak_source": peaks_src,
-                     "tflops": tf,
-                     "tensor_frac": tf / peaks.get("bf16_tflops_sustained", 1700.0)},
-        # sparse: the gathered-attention kernel, plus the merge when lists are split
-        "gpu_launches": args.steps * (2 if args.workload == "block"
-                                      else 4 if args.workload == "select"
-                                      else 2 if args.workload == "index" or nb > 0 else 1),
-        "clocks": clk.summary(),
+                   "launch": "CUDA graph replay" if graphed else "direct",
+                   "timing": "median of %d steps (ms_mean beside it); warm_l2_ms: the same "
+                             "steps back to back, no flush" % args.steps},
+        "roofline": rec["roofline"],
+        "ms_mean": rec["ms_mean"], "warm_l2_ms": rec["warm_l2_ms"],
+        "gpu_launches": args.steps * p.launches,
+        "clocks": summ,
     }
+
+
+def measure_paths(names, rank, world, device, peaks, peaks_src, steps=50, warmup=5):
+    """The `paths` record of the default line: each named path measured in the
+    same run (median of `steps` timed steps after `warmup`)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    out = {}
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    for name in names:
+        p = build_path(name, rank_seed(rank), device, stream)
+        cold, warm, graphed = time_path(p, steps, warmup, stream, world)
+        rec = path_record(p, cold, warm, peaks, peaks_src, world, None, sms)
+        rec["workload"] = p.name
+        rec["launch"] = "CUDA graph replay, L2 flushed" if graphed else "direct"
+        out[name] = rec
+        del p
+        torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------- reference arm
@@ -648,8 +738,9 @@ def run_reference(args, rank, world):
             "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64, bf16 inputs)",
-            "config": {"workload": "window-vision-bf16: %d seqs U{64..1024}, H=16, Hkv in "
-                                   "{16,8}, d=128, w=128 (oracle sample)"},
+            "config": {"workload": "window-vision-bf16: 256 seqs U{64..1024}, H=16, Hkv in "
+                                   "{16,8}, d=128, w=128 (oracle sample: two sequences of the "
+                                   "Hkv=16 key0_bias pass per step)"},
             "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0,
@@ -712,6 +803,8 @@ def main():
                     help="window workload: number of sequences (256 = the full workload)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-paths", action="store_true",
+                    help="window workload: skip the decode / prefill / block-sparse sub-record")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

@@ -7,18 +7,16 @@
  * host memory. Its state: on the host, a per-device cache of attributes and
  * device addresses, the tensor-map encoder entry point, the debug flag and
  * wait limit, and a launch counter; on each device, module-scope arrays built
- * into the library: the error word, a ring of 256 item-claim words and the
+ * into the library: the error word, a ring of 256 item-claim counters and the
  * scratch array of sattn_sparse_fwd_static_scratch.
  *
- * Claim words: each launch of the window and block-sparse kernels takes the
- * next word of the ring (zeroed on its stream) and tags it with a per-launch
- * number; its CTAs claim work items from it. A launch that finds the word
- * tagged by another launch (two launches 256 apart in issue order that
- * overlap on the GPU, e.g. on different streams or in concurrently replayed
- * CUDA graphs) never modifies it and takes its remaining items in a static
- * order instead: results stay exact, only the load balance suffers. Replaying
- * ONE captured graph concurrently with itself is not supported (it also
- * writes the same output buffers).
+ * Claim counters: each call of sattn_window_fwd, sattn_block_sparse_fwd and
+ * sattn_block_sparse_chunks_fwd takes the next counter of the ring (zeroed
+ * on its stream by an asynchronous memset) and its CTAs claim work items
+ * from it. LIMIT: two such calls 256 calls apart in issue order use the same
+ * counter and must not run at the same time on the GPU (different streams,
+ * or CUDA graphs that captured them replayed concurrently); keep fewer than
+ * 256 of these calls in flight at once. Calls on one stream never overlap.
  *
  * Execution: every compute call is asynchronous on `cuda_stream` (a
  * cudaStream_t; NULL selects the per-thread default stream, never the legacy

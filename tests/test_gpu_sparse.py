@@ -165,8 +165,11 @@ def _decode_inputs(case):
 
 def test_split_merge_reuses_a_workspace_and_ignores_its_contents():
     # split lists: a workspace full of random bytes, then the same workspace
-    # again and again, all give the oracle's result and the same bits
-    case = W.sparse_decode_bf16(11, B=16)
+    # again and again, all give the oracle's result and the same bits. 100
+    # queries of 640 entries are too many for one cluster per query on 152
+    # SMs (a CTA holds at most 384 entries), so the persistent kernel splits
+    # the lists through the workspace
+    case = W.sparse_decode_bf16(11, B=100)
     q, kv, idx, s, nb = _decode_inputs(case)
     ws = torch.randint(0, 256, (nb,), dtype=torch.uint8, device="cuda")
     ro, rl = oracle_sparse(case)
@@ -183,8 +186,8 @@ def test_split_merge_reuses_a_workspace_and_ignores_its_contents():
 
 def test_split_merge_under_graph_replay():
     # a captured split call (the gathered kernel and the merge) gives the
-    # oracle's result on every replay
-    case = W.sparse_decode_bf16(12, B=32)
+    # oracle's result on every replay (100 queries: the split path, as above)
+    case = W.sparse_decode_bf16(12, B=100)
     q, kv, idx, s, nb = _decode_inputs(case)
     ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
     o = torch.empty((case.B, case.M, case.H, case.d), dtype=torch.bfloat16, device="cuda")
@@ -206,3 +209,51 @@ def test_split_merge_under_graph_replay():
         torch.cuda.synchronize()
         sa.check_device()
         compare(o, lse, ro, rl, TOL_BF16_O, what="replay %d" % it)
+
+
+@pytest.mark.parametrize("B,K", [(1, 3072), (2, 1), (3, 100), (5, 383), (8, 0), (19, 700),
+                                 (38, 384), (64, 640), (76, 768), (77, 384)])
+def test_decode_clusters(B, K):
+    """Few queries: each list is cut into C = 1..8 segments, one CTA of a
+    cluster each, merged through distributed shared memory. Lists of every
+    length the kernel takes (up to 3 tiles per CTA), -1 entries, empty
+    segments (K < C), a list with nothing valid, all three sink modes."""
+    rng = np.random.default_rng(B * 1000 + K)
+    M, H, d, N = 1, 32, 128, 5000
+    q = W.round_bf16(rng.standard_normal((B, M, H, d)).astype(np.float32))
+    kv = W.round_bf16(rng.standard_normal((B, N, d)).astype(np.float32))
+    idx = rng.integers(0, N, size=(B, M, K)).astype(np.int32)
+    if K:
+        idx[rng.random((B, M, K)) < 0.15] = -1
+        idx[0, 0, : min(K, 7)] = 0  # key 0 for the key-0 bias (seven times)
+        if B > 1:
+            idx[B - 1, 0, :] = -1  # a query that sees nothing
+    case = W.SparseCase(q=q, kv=kv, idx=idx, sinks=rng.standard_normal(H).astype(np.float32),
+                        scale=d ** -0.5)
+    for mode in (0, 1, 2):
+        o, lse = run_sparse(case, mode, workspace=False)
+        ro, rl = oracle_sparse(case, mode)
+        compare(o, lse, ro, rl, TOL_BF16_O, what="B=%d K=%d mode=%d" % (B, K, mode))
+
+
+def test_decode_gather_decisions_bit_exact():
+    """The cluster path's visible sets: q = 0, row n = e_(n mod 128); with
+    |S| <= 128 per query the support of o recovers every valid entry."""
+    B, M, H, d, N, K = 4, 1, 32, 128, 128, 700
+    rng = np.random.default_rng(19)
+    q = np.zeros((B, M, H, d), np.float32)
+    kv = np.zeros((B, N, d), np.float32)
+    for n in range(N):
+        kv[:, n, n % d] = 1.0
+    idx = np.full((B, M, K), -1, np.int32)
+    for b in range(B):  # a handful of valid entries scattered over the segments
+        pos = rng.choice(K, size=40, replace=False)
+        idx[b, 0, pos] = rng.integers(0, N, size=40)
+    case = W.SparseCase(q=q, kv=kv, idx=idx, sinks=rng.standard_normal(H).astype(np.float32),
+                        scale=d ** -0.5)
+    for mode in (0, 1, 2):
+        o, lse = run_sparse(case, mode, workspace=False)
+        ro, rl = oracle_sparse(case, mode)
+        got = o.float().cpu().numpy().reshape(ro.shape) != 0
+        assert np.array_equal(got, ro != 0), mode
+        compare(o, lse, ro, rl, TOL_BF16_O)

@@ -55,8 +55,10 @@ def _static_call(case, q, kv, idx, sinks):
 
 def test_static_scratch_matches_workspace_entry_point():
     for seed in (0, 1):  # two calls in a row, with different inputs
-        # short lists for few requests: the call splits each list across CTAs
-        case = W.sparse_decode_bf16(seed, B=8)
+        # 100 requests of 512 entries: more queries than one cluster per query
+        # can hold on 152 SMs, so the call splits each list across the CTAs of
+        # the persistent kernel, with the partials in the scratch array
+        case = W.sparse_decode_bf16(seed, B=100, n_compress_idx=384)
         need = sa.sparse_workspace_bytes(case.B, case.M, case.H, case.d, case.K)
         assert 0 < need <= STATIC_SCRATCH_BYTES
         q, kv, idx, sinks = _tensors(case)

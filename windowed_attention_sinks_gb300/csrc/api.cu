@@ -17,10 +17,10 @@
 namespace sattn {
 
 __device__ unsigned g_error_word;
-// Item-claim words of the persistent kernels, one per launch in turn, each on
-// its own 128-byte line.
-constexpr unsigned kClaimStride = 16;
-__device__ unsigned long long g_claims[kClaimWords * kClaimStride];
+// Item-claim counters of the persistent kernels, one per launch in turn, each
+// on its own 128-byte line.
+constexpr unsigned kClaimStride = 32;
+__device__ unsigned g_claims[kClaimCounters * kClaimStride];
 
 namespace {
 
@@ -80,7 +80,7 @@ const DevInfo *device_info(cudaError_t *e) {
         if ((*e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return nullptr;
         d.err = static_cast<unsigned *>(p);
         if ((*e = cudaGetSymbolAddress(&p, g_claims)) != cudaSuccess) return nullptr;
-        d.claims = static_cast<unsigned long long *>(p);
+        d.claims = static_cast<unsigned *>(p);
         if ((*e = cudaMemset(d.err, 0, sizeof(unsigned))) != cudaSuccess) return nullptr;
         if ((*e = cudaDeviceSynchronize()) != cudaSuccess) return nullptr;
         g_dev[dev] = d;
@@ -91,14 +91,11 @@ const DevInfo *device_info(cudaError_t *e) {
 
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
 
-unsigned long long *launch_claim_word(const DevInfo &dev, cudaStream_t s, unsigned *tag,
-                                      cudaError_t *e) {
+unsigned *launch_claim_counter(const DevInfo &dev, cudaStream_t s, cudaError_t *e) {
     static std::atomic<unsigned> next{0};
-    const unsigned n = next.fetch_add(1);
-    *tag = n % 0xffffffffu + 1u;  // never 0: a zero word is free
-    unsigned long long *w = dev.claims + (size_t)(n % kClaimWords) * kClaimStride;
-    *e = cudaMemsetAsync(w, 0, sizeof(*w), s);
-    return *e == cudaSuccess ? w : nullptr;
+    unsigned *c = dev.claims + (size_t)(next.fetch_add(1) % kClaimCounters) * kClaimStride;
+    *e = cudaMemsetAsync(c, 0, sizeof(*c), s);
+    return *e == cudaSuccess ? c : nullptr;
 }
 
 cudaError_t ensure_smem_attr(const void *kernel, size_t bytes, const DevInfo &dev) {

@@ -85,8 +85,7 @@ struct TcParams {
     int M, Nctx, q_pos0, kv_begin, kv_end, QB, KB;
     int chunk_keys;        // [kv_begin, kv_end) in chunks of this many keys, one output each
     float *o_part, *lse_part;  // [chunk, M, H, d] and [chunk, M, H]
-    unsigned long long *work;  // the launch's claim word (tag << 32 | items claimed)
-    unsigned work_tag;
+    unsigned *work;  // the launch's claim counter, zeroed on its stream: items claimed
 };
 
 struct Item {
@@ -102,44 +101,6 @@ struct Item {
     int kb_lo, kb_hi, kend;  // block: 128-key block range, key limit
     float sink;              // window: the head's sink (0 when there is none)
 };
-
-// Dynamic item claims on the launch's claim word (tag << 32 | count; zero
-// means free). The caller keeps its last view of the word in `seen`. Returns
-// the claimed index, or -1 when the word carries another launch's tag: an
-// overlapping launch reused the ring entry, and this slot then takes the rest
-// of its items from a static schedule. A word of another launch is never
-// modified, so neither launch loses or repeats items of the other.
-__device__ __forceinline__ int claim_item(unsigned long long *w, unsigned tag,
-                                          unsigned long long &seen) {
-    for (;;) {
-        unsigned long long want;
-        int got;
-        if (seen == 0ull) {  // free: this claim opens the launch's count
-            want = ((unsigned long long)tag << 32) | 1ull;
-            got = 0;
-        } else if ((unsigned)(seen >> 32) == tag) {
-            want = seen + 1ull;
-            got = (int)(unsigned)seen;
-        } else {
-            return -1;
-        }
-        const unsigned long long prev = atomicCAS(w, seen, want);
-        if (prev == seen) return got;
-        seen = prev;
-    }
-}
-// Move the launch's count forward to `target` (items below it need no claim);
-// nothing if the word is free or another launch's.
-__device__ __forceinline__ void claim_skip_to(unsigned long long *w, unsigned tag,
-                                              unsigned target, unsigned long long &seen) {
-    for (;;) {
-        if ((unsigned)(seen >> 32) != tag || (unsigned)seen >= target) return;
-        const unsigned long long prev =
-            atomicCAS(w, seen, ((unsigned long long)tag << 32) | target);
-        if (prev == seen) return;
-        seen = prev;
-    }
-}
 
 struct Bars {
     uint64_t q_full, q_empty, k_full[KSTAGES], k_empty[KSTAGES], v_full[VSTAGES], v_empty[VSTAGES];
@@ -332,33 +293,24 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
     const int v_static =
         MODE == MODE_WINDOW ? (p.num_items / 8 * 7 / stride) * stride : 0;
     int v_next = first;  // next round-robin item
-    bool claims = true;  // false: the claim word was taken over, static schedule
-    unsigned long long seen = 0ull;
     for (;;) {
         int v;
-        if (v_next < v_static || !claims) {
+        if (v_next < v_static) {
             v = v_next;
             v_next += stride;
-            if (v >= p.num_items) break;
         } else {
-            const int c = claim_item(p.work, p.work_tag, seen);
-            if (c < 0) {  // v_next is v_static + first here: this slot's share
-                claims = false;
-                continue;
-            }
-            v = v_static + c;
+            v = v_static + (int)atomicAdd(p.work, 1u);
             if (v >= p.num_items) break;
         }
         const Item it = decode_item<MODE>(p, v);
         if (!it.valid) {
             if (it.seq_err) {
                 record_error(ctx, DEVERR_SEQLENS);
-            } else if (MODE == MODE_WINDOW && v >= v_static && claims) {
+            } else if (MODE == MODE_WINDOW && v >= v_static) {
                 // every later item of this sequence lies past its end as well:
-                // move the count to the next sequence's first item
+                // move the counter to the next sequence's first item
                 const int per_seq = p.H * p.tiles_per_seq;
-                claim_skip_to(p.work, p.work_tag,
-                              (unsigned)((v / per_seq + 1) * per_seq - v_static), seen);
+                atomicMax(p.work, (unsigned)((v / per_seq + 1) * per_seq - v_static));
             }
             continue;
         }
@@ -848,7 +800,7 @@ template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int 
     if (e != cudaSuccess) return e;
     const int streams = (p.num_items + NSLOTS - 1) / NSLOTS;
     const int grid = streams < dev.sm_count ? streams : dev.sm_count;
-    if (!(p.work = launch_claim_word(dev, s, &p.work_tag, &e))) return e;
+    if (!(p.work = launch_claim_counter(dev, s, &e))) return e;
     DevCtx ctx{dev.err, wait_limit_ns()};
     if (verbose())
         fprintf(stderr, "sattn: attn_tc_kernel<%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",

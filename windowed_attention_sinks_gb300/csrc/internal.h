@@ -16,27 +16,22 @@ struct DevInfo {
     int sm_count = 0;
     int cc_major = 0, cc_minor = 0;
     unsigned *err = nullptr;                 // device address of the error word
-    unsigned long long *claims = nullptr;    // device address of the claim-word ring
+    unsigned *claims = nullptr;              // device address of the claim-counter ring
 };
 
 // Per-device facts, initialised once per device (thread-safe).
 const DevInfo *device_info(cudaError_t *e);
 uint64_t wait_limit_ns();
 
-// The item-claim word of one launch of a persistent kernel that hands out
-// work items dynamically. The word holds (tag << 32 | items claimed); the
-// launch's tag is unique among the last 2^32 - 1 launches. The word is the
-// next of a ring of kClaimWords built into the library and is zeroed by an
-// asynchronous memset on `s`. A kernel claims by compare-and-swap and never
-// modifies a word that carries another launch's tag (zero counts as free);
-// when it finds one, because an overlapping launch reused the ring entry, it
-// switches to a static schedule of the remaining items. Overlapping launches
-// therefore never lose or repeat each other's items; sharing an entry only
-// costs the dynamic balancing. Returns nullptr (and sets *e) if the memset
-// cannot be issued.
-constexpr unsigned kClaimWords = 256;
-unsigned long long *launch_claim_word(const DevInfo &dev, cudaStream_t s, unsigned *tag,
-                                      cudaError_t *e);
+// The item-claim counter of one launch of a persistent kernel that hands
+// out work items dynamically: the next of a ring of kClaimCounters built into
+// the library (each on its own 128-byte line), zeroed by an asynchronous
+// memset on `s`. Two launches that get the same counter (kClaimCounters
+// launches apart in issue order) must not overlap on the GPU; the header
+// states this limit. Returns nullptr (and sets *e) if the memset cannot be
+// issued.
+constexpr unsigned kClaimCounters = 256;
+unsigned *launch_claim_counter(const DevInfo &dev, cudaStream_t s, cudaError_t *e);
 
 // cudaFuncSetAttribute(kernel, MaxDynamicSharedMemorySize, bytes) once per
 // (kernel, device, size), thread-safe.
@@ -150,6 +145,11 @@ cudaError_t launch_merge(const MergeArgs &a, const DevInfo &dev, cudaStream_t s,
 cudaError_t launch_window_tc(const WindowArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t s);
 cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
+// Few queries: each query's list cut into C segments, one per CTA of a
+// cluster, merged through distributed shared memory. Returns the cluster
+// size C for a shape this kernel takes (bf16, H = 32, d = 128), else 0.
+int sparse_decode_cluster(int B, int M, int K, int sm_count);
+cudaError_t launch_sparse_decode(const SparseArgs &a, int C, const DevInfo &dev, cudaStream_t s);
 size_t sparse_tc_workspace_bytes(int B, int M, int H, int d, int K);
 
 }  // namespace sattn

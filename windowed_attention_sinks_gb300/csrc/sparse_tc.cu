@@ -41,18 +41,18 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "sparse_layout.cuh"
 
 namespace sattn {
 namespace {
 
-constexpr int R = 128;         // gathered rows per tile
-constexpr int HD = 128;        // head dim
-constexpr int NH = 32;         // query heads handled by the kernel
+using namespace gather;
+
 constexpr int NSLOT = 2;         // independent item streams per CTA
 // Per slot: one warp compacts index lists, GATHER_WARPS warps copy rows (one
 // warp issues cp.async at ~10 B/clk at most, and index loads queued behind a
 // warp's copies would stall its compaction), one warp issues the MMAs.
-constexpr int GATHER_WARPS = 4;
+constexpr int GATHER_WARPS = COPY_WARPS;
 constexpr int SLOT_CTRL = GATHER_WARPS + 2;  // control warps of a slot
 // Compacted-index ring depth: the lead warp runs up to IDX_RING - 1 tiles
 // ahead of the slowest reader of the ring (copy warps, MMA, softmax warps),
@@ -63,13 +63,6 @@ constexpr int LCHUNK = 256;
 constexpr int NLCH = 2;
 constexpr int NTHREADS = 32 * NSLOT * (SLOT_CTRL + 4);
 constexpr int SOFTMAX_THREADS = 128;
-constexpr uint32_t KV_TILE = R * HD * 2;   // 32 KB
-constexpr uint32_t KV_HALF = KV_TILE / 2;  // 64 columns of d
-constexpr uint32_t QP_HALF = NH * 128;     // 4 KB: one 64-column half of Q or P
-// Per-warp transpose buffer: head h, key i of the warp at h * TB_STRIDE + i.
-// Writes (one head, 32 keys) are consecutive; the 16-byte reads of the 8
-// lanes sharing an LDS.128 phase fall in distinct bank groups (9h + k mod 8).
-constexpr int TB_STRIDE = 36;
 constexpr float TAU = 8.0f;
 constexpr int MAX_SPLITS = 64;
 constexpr uint32_t SLOT_COLS = 128;  // TMEM per slot: S^T[2] (32 each), O^T (32)
@@ -132,22 +125,6 @@ struct SpParams {
     float *o_part, *lse_part;  // workspace (splits > 1)
 };
 
-constexpr uint32_t IDESC_S = idesc_bf16_f32(128, NH, 0, 0);
-constexpr uint32_t IDESC_O = idesc_bf16_f32(128, NH, 1, 0);
-
-// Shared-memory descriptors are built once per buffer; the K step kk (16
-// elements) only moves the start address, whose field holds address >> 4 in
-// the low bits (no carry: shared addresses stay below 256 KB).
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t base, uint32_t lbo) {
-    return smem_desc_sw128(base, lbo, 1024u);
-}
-// K-major operand split in 64-element halves `half_stride` bytes apart
-__host__ __device__ constexpr uint32_t koff(int kk, uint32_t half_stride) {
-    return ((uint32_t)(kk >> 2) * half_stride + (uint32_t)(kk & 3) * 32u) >> 4;
-}
-// MN-major operand: 16 K rows of 128 bytes per step
-__host__ __device__ constexpr uint32_t mnoff(int kk) { return (uint32_t)kk * 2048u >> 4; }
-
 // 2-D tiled TMA load (x = column, y = row), completion on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, uint32_t bar,
                                             int x, int y) {
@@ -157,17 +134,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *m, 
         "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
         : "memory");
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-// Arrive on `bar` once every cp.async this thread issued so far has landed
-// (counts as one of the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
 // Barrier among the slot's four softmax warps (named barrier 1 + slot) that
 // also returns whether any thread's predicate was true.
 __device__ __forceinline__ int softmax_sync_or(int slot, int pred) {
@@ -199,41 +165,10 @@ __device__ __forceinline__ ItemInfo item_info(const SpParams &p, int item) {
 
 // ------------------------------------------------------------------ gather warp
 
-// Copy warp g of a slot copies rows 2i + hi, i in [PAIRS g, PAIRS (g+1)), of
-// each tile. The lead warp loads Q, compacts the index lists into the ring
-// and publishes each ring entry to the copy warps, the MMA and the softmax
-// warps (idx_ready); after the last tile it publishes an entry with
-// tile_row0 = -1.
-constexpr int PAIRS = R / 2 / GATHER_WARPS;  // row pairs per warp (multiple of 4)
-
-struct RowCopier {
-    uint32_t dofs[4];
-    int hi, unit;
-    // lane = (hi, unit) copies 16-byte unit `unit` of rows 2i + hi. In the 128B
-    // swizzle, unit u of row r sits at r * 128 + ((u ^ (r & 7)) << 4), and
-    // (unit & 7) ^ (r & 7) = ((unit & 7) ^ hi) ^ (2i & 6): four lane offsets
-    // cover every i.
-    __device__ explicit RowCopier(int lane) {
-        hi = lane >> 4;
-        unit = lane & 15;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-            dofs[c] = (uint32_t)(unit >> 3) * KV_HALF + (uint32_t)hi * 128u +
-                      ((((uint32_t)(unit & 7) ^ (uint32_t)hi) ^ (uint32_t)(2 * c)) << 4);
-    }
-    // this warp's rows of one tile; entries of -1 are zero-filled so that P V
-    // stays finite
-    __device__ void issue(uint32_t kv_s, const int *ids, const __nv_bfloat16 *rows, int g) const {
-        const __nv_bfloat16 *src0 = rows + unit * 8;
-#pragma unroll
-        for (int i2 = 0; i2 < PAIRS; ++i2) {
-            const int i = PAIRS * g + i2;
-            const int e = ids[2 * i + hi];
-            cp_async16(kv_s + dofs[i2 & 3] + (uint32_t)i * 256u,
-                       src0 + (size_t)(e >= 0 ? e : 0) * HD, e >= 0 ? 16u : 0u);
-        }
-    }
-};
+// Copy warp g of a slot copies rows 32 g .. 32 g + 31 of each tile (RowCopier).
+// The lead warp loads Q, compacts the index lists into the ring and publishes
+// each ring entry to the copy warps, the MMA and the softmax warps
+// (idx_ready); after the last tile it publishes an entry with tile_row0 = -1.
 
 // FP8 cache rows: the RoPE part (bf16, the stage's second 64-column half) is
 // copied by cp.async like the bf16 rows; the DN e4m3 codes are loaded to
@@ -975,6 +910,14 @@ size_t sparse_tc_workspace_bytes(int B, int M, int H, int d, int K) {
 cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream_t s) {
     const bool fp8 = a.kv == nullptr;
     if (a.H != NH || a.d != HD) return fp8 ? cudaErrorInvalidValue : launch_sparse_simt(a, dev, s);
+    if (!fp8) {  // few queries: one launch, splits merged inside clusters
+        const int C = sparse_decode_cluster(a.B, a.M, a.K, dev.sm_count);
+        if (C > 0) {
+            const cudaError_t e = launch_sparse_decode(a, C, dev, s);
+            if (e != cudaErrorInvalidClusterSize) return e;
+            (void)cudaGetLastError();  // nothing was launched: take the split path
+        }
+    }
     SpParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.kv = static_cast<const __nv_bfloat16 *>(a.kv);
