@@ -416,6 +416,18 @@ sattn_status sattn_check_device(void *cuda_stream);
  * one second). A value of 0 restores the default. */
 void sattn_set_wait_limit_ns(uint64_t ns);
 
+/* Test hook for the failure path of the tensor-core kernels (window,
+ * block-sparse, gathered, gathered FP8, block-selection stats and sums). With
+ * `on` nonzero, launches made afterwards start with their MMA-issuing thread
+ * waiting for a barrier phase that nothing completes: that wait runs out
+ * after the wait limit, the kernel records SATTN_ERR_TIMEOUT in the device
+ * error word, stops every role of the CTA, lets its own copies and MMAs in
+ * flight finish (bounded) and frees its tensor memory. The outputs of such a
+ * launch are undefined; nothing faults, traps or hangs. 0 (the default) turns
+ * the hook off. Keep the wait limit short while it is on (a few
+ * milliseconds: every launch then takes about that long). */
+void sattn_set_test_wait_stall(int on);
+
 /* Library ABI version (major * 100 + minor). */
 int32_t sattn_version(void);
 

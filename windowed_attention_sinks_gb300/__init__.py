@@ -94,6 +94,8 @@ def lib() -> ctypes.CDLL:
     L.sattn_check_device.restype = ctypes.c_int
     L.sattn_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     L.sattn_set_wait_limit_ns.restype = None
+    L.sattn_set_test_wait_stall.argtypes = [ctypes.c_int]
+    L.sattn_set_test_wait_stall.restype = None
     L.sattn_version.restype = i32
     _lib = L
     return L
@@ -500,3 +502,14 @@ def check_device(stream=None):
 
 def set_debug(on: bool):
     lib().sattn_set_debug(1 if on else 0)
+
+
+def set_wait_limit_ns(ns: int):
+    """Bound on any single wait inside a kernel (sattn_set_wait_limit_ns); 0 = default."""
+    lib().sattn_set_wait_limit_ns(int(ns))
+
+
+def set_test_wait_stall(on: bool):
+    """Test hook (sattn_set_test_wait_stall): later tensor-core launches take
+    their timeout path; outputs undefined, SATTN_ERR_TIMEOUT recorded."""
+    lib().sattn_set_test_wait_stall(1 if on else 0)

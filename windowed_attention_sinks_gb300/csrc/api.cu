@@ -30,6 +30,7 @@ DevInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices];
 std::atomic<int> g_debug{0};
 std::atomic<uint64_t> g_wait_ns{1000000000ull};
+std::atomic<int> g_test_stall{0};
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -90,6 +91,8 @@ const DevInfo *device_info(cudaError_t *e) {
 }
 
 uint64_t wait_limit_ns() { return g_wait_ns.load(); }
+
+DevCtx make_ctx(const DevInfo &dev) { return DevCtx{dev.err, g_wait_ns.load(), g_test_stall.load()}; }
 
 unsigned *launch_claim_counter(const DevInfo &dev, cudaStream_t s, cudaError_t *e) {
     static std::atomic<unsigned> next{0};
@@ -187,6 +190,8 @@ const char *sattn_status_str(sattn_status s) {
 void sattn_set_debug(int on) { g_debug.store(on ? 1 : 0); }
 
 void sattn_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns ? ns : 1000000000ull); }
+
+void sattn_set_test_wait_stall(int on) { g_test_stall.store(on ? 1 : 0); }
 
 sattn_status sattn_check_device(void *cuda_stream) {
     cudaError_t e;

@@ -338,8 +338,10 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
         Item end{};  // valid = false: no more items
         ok = publish(end);
     }
-    if (!ok) {
-        // Let copies already in flight land before the CTA leaves (bounded).
+    {
+        // Let copies already in flight land before the CTA leaves (bounded;
+        // on the normal path every phase waited for here has completed, and
+        // after an abort of another role loads may still be in flight).
         int zero = 0;
         if (qi > 0) mbar_wait(smem_u32(&b.q_full), (qi - 1) & 1, ctx, &zero);
         for (int i = 1; i <= KSTAGES && i <= kt; ++i)
@@ -364,6 +366,7 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
     const uint64_t dk1 = smem_desc_sw128(smem_u32(sm.k[1]), 16u, 1024u);
     const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), KV_HALF, 1024u);
     const uint64_t dv1 = smem_desc_sw128(smem_u32(sm.v[1]), KV_HALF, 1024u);
+    if (ctx.stall) mbar_wait(smem_u32(&b.drain), 0, ctx, abort);  // test hook: runs out
     for (int ic = 0; ok; ++ic) {
         const int slot_k = ic % ITEM_RING;
         if (!mbar_wait(smem_u32(&b.item_full[slot_k]), (ic / ITEM_RING) & 1, ctx, abort)) break;
@@ -801,7 +804,7 @@ template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int 
     const int streams = (p.num_items + NSLOTS - 1) / NSLOTS;
     const int grid = streams < dev.sm_count ? streams : dev.sm_count;
     if (!(p.work = launch_claim_counter(dev, s, &e))) return e;
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     if (verbose())
         fprintf(stderr, "sattn: attn_tc_kernel<%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",
                 MODE == MODE_WINDOW ? "window" : "block", grid, NTHREADS, smem, NSLOTS,

@@ -101,7 +101,7 @@ cudaError_t launch_topk_idxs(int32_t *out, const int32_t *start_pos, int B, int 
     if (total > 0x7fffffffLL - 256) return cudaErrorInvalidValue;  // 32-bit thread index
     const int threads = 256;
     const int blocks = (int)((total + threads - 1) / threads);
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     topk_idxs_kernel<<<blocks, threads, 0, s>>>(out, start_pos, M, K, win, ratio, warps_per_row,
                                                 (int)total, ctx);
     return cudaGetLastError();
@@ -117,7 +117,7 @@ cudaError_t launch_kv_ring_write(void *cache, const void *src, const int32_t *st
     const int threads = 256;
     const long long blocks = (total16 + threads - 1) / threads;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     ring_write_kernel<<<(unsigned)blocks, threads, 0, s>>>(
         static_cast<uint8_t *>(cache), static_cast<const uint8_t *>(src), start_pos, S, N, n, win,
         row_bytes, total16, ctx);

@@ -26,6 +26,10 @@ constexpr float LN2 = 0.6931471805599453f;
 struct DevCtx {
     unsigned *err;       // device error word
     uint64_t wait_ns;    // bound on a single wait
+    // test hook: the MMA-issuing thread of each tensor-core kernel first
+    // waits for a barrier phase that nothing completes, so the bounded wait
+    // runs out and the kernel takes its abort path (see sattn_set_test_wait_stall)
+    int stall;
 };
 
 // ----------------------------------------------------------------- math
@@ -135,13 +139,22 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t smem_addr, uint32_t rank
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void st_dsmem4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
+// Asynchronous stores into the shared memory of a CTA of the cluster (cluster
+// addresses from dsmem_addr); their bytes are counted on that CTA's mbarrier
+// `mbar` (also a cluster address), which the receiver waits on.
+__device__ __forceinline__ void st_async(uint32_t addr, float v, uint32_t mbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+                     addr),
+                 "f"(v), "r"(mbar)
                  : "memory");
+}
+__device__ __forceinline__ void st_async4(uint32_t addr, float a, float b, float c, float d,
+                                          uint32_t mbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+            addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar)
+        : "memory");
 }
 
 // ----------------------------------------------------------------- mbarrier

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "sattn.h"
+#include "common.cuh"
 
 namespace sattn {
 
@@ -22,6 +23,8 @@ struct DevInfo {
 // Per-device facts, initialised once per device (thread-safe).
 const DevInfo *device_info(cudaError_t *e);
 uint64_t wait_limit_ns();
+// The device context of one launch: error word, wait limit, test stall flag.
+struct DevCtx make_ctx(const DevInfo &dev);
 
 // The item-claim counter of one launch of a persistent kernel that hands
 // out work items dynamically: the next of a ring of kClaimCounters built into

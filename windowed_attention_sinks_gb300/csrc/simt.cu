@@ -311,7 +311,7 @@ inline dim3 rows_grid(int64_t rows) { return dim3((unsigned)((rows + kWarps - 1)
 }  // namespace
 
 cudaError_t launch_window_simt(const WindowArgs &a, const DevInfo &dev, cudaStream_t s) {
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     dim3 g = rows_grid((int64_t)a.T * a.H), b(kWarps * 32);
     if (a.dtype == SATTN_F32) {
         if (a.d == 64) window_simt_kernel<float, 64><<<g, b, 0, s>>>(a, ctx);
@@ -324,7 +324,7 @@ cudaError_t launch_window_simt(const WindowArgs &a, const DevInfo &dev, cudaStre
 }
 
 cudaError_t launch_sparse_simt(const SparseArgs &a, const DevInfo &dev, cudaStream_t s) {
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     dim3 g = rows_grid((int64_t)a.B * a.M * a.H), b(kWarps * 32);
     if (a.dtype == SATTN_F32) {
         if (a.d == 64) sparse_simt_kernel<float, 64><<<g, b, 0, s>>>(a, ctx);
@@ -337,7 +337,7 @@ cudaError_t launch_sparse_simt(const SparseArgs &a, const DevInfo &dev, cudaStre
 }
 
 cudaError_t launch_block_simt(const BlockArgs &a, const DevInfo &dev, cudaStream_t s) {
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     dim3 g = rows_grid((int64_t)a.M * a.H), b(kWarps * 32);
     if (a.dtype == SATTN_F32) {
         if (a.d == 64) block_simt_kernel<float, 64><<<g, b, 0, s>>>(a, ctx);

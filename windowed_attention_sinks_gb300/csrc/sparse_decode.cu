@@ -19,11 +19,11 @@
 //   - accumulates O^T += KV^T P^T over the tiles,
 //   - leaves its partial (m, l, O^T) in shared memory.
 // CTA r of the cluster owns heads [r 32/C, (r+1) 32/C) of the query: every
-// CTA stores its partial of those heads (O^T rows, m, l) straight into CTA
-// r's shared memory (distributed shared memory stores, no round trip), and
-// after one cluster barrier each CTA merges its heads from its own shared
-// memory through the log-sum-exp (the null-logit sink is added here, once)
-// and writes o and lse. One launch, no workspace.
+// CTA sends its partial of those heads (O^T rows, m, l) straight into CTA
+// r's shared memory with asynchronous stores whose bytes complete on CTA
+// r's own mbarrier, so a CTA starts merging as soon as its heads' partials
+// have landed. It merges them through the log-sum-exp (the null-logit sink
+// is added here, once) and writes o and lse. One launch, no workspace.
 //
 // Warps 0-3: Q copy, softmax, epilogue and merge (warp w reads TMEM lanes
 // 32w .. 32w+31); warps 4-7: row copies (warp 4 + g: rows 32g .. 32g+31 of
@@ -54,7 +54,12 @@ struct DecBars {
     uint64_t q_full;
     uint64_t kv_full[DT_MAX], s_full[DT_MAX], p_full[DT_MAX];
     uint64_t o_full, drain;
+    uint64_t recv_full;  // every CTA's partial of this CTA's heads has landed (tx bytes)
 };
+
+// Bytes a CTA receives: from each of the C CTAs, HD rows of hs = NH / C O^T
+// values and hs (m, l) pairs; C hs = NH.
+constexpr uint32_t RECV_BYTES = NH * (HD * 4 + 8);
 
 struct alignas(1024) DecSmem {
     uint8_t kv[DT_MAX][KV_TILE];
@@ -98,6 +103,7 @@ __device__ __forceinline__ void softmax_bar() {
 
 __device__ void dec_mma(const DecSmem &sm, DecBars &b, uint32_t tmem, int nt, volatile int *abort,
                         const DevCtx &ctx) {
+    if (ctx.stall) mbar_wait(smem_u32(&b.drain), 0, ctx, abort);  // test hook: runs out
     bool ok = nt > 0 && mbar_wait(smem_u32(&b.q_full), 0, ctx, abort);
     const uint64_t dq = desc_sw128(smem_u32(sm.q), 16u);
     int issued = 0;
@@ -176,6 +182,8 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
         }
         mbar_init(smem_u32(&b.o_full), 1);
         mbar_init(smem_u32(&b.drain), 1);
+        mbar_init(smem_u32(&b.recv_full), 1);
+        mbar_arrive_expect_tx(smem_u32(&b.recv_full), RECV_BYTES);
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -186,8 +194,10 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // first cluster phase: every CTA of the cluster has started (waited for
-    // before the first store into another CTA's shared memory)
+    // first cluster phase: every CTA of the cluster has started and set up its
+    // barriers (waited for before the first store into another CTA's shared
+    // memory); the second, at the end, keeps every CTA alive until all the
+    // cluster's stores into it have landed
     cluster_arrive_relaxed();
     const uint32_t tmem = sm.tmem_base;
     volatile int *abort = &sm.abort;
@@ -217,9 +227,9 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
             __syncwarp();
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-        cluster_wait_acquire();
         tc_fence_before();  // the MMAs drained above come before the dealloc
-        cluster_arrive_release();
+        cluster_wait_acquire();
+        cluster_arrive_relaxed();
         cluster_wait_acquire();
     } else {
         // ---- softmax over the segment (lane = head after the transpose)
@@ -343,33 +353,37 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
         }
         // the Q copies have landed (a CTA without tiles never waited for them)
         asm volatile("cp.async.wait_all;" ::: "memory");
-        // ---- push: heads of CTA r go to CTA r's shared memory
+        // ---- send: heads of CTA r go to CTA r's shared memory
         const int hs = NH / C;
-        cluster_wait_acquire();  // every CTA of the cluster is running
+        cluster_wait_acquire();  // every CTA of the cluster is running, its barriers set up
         {
             const int d = quarter * 32 + lane;
             const uint32_t row = smem_u32(sm.recv) +
                                  (uint32_t)(((int)crank * HD + d) * (hs + 4)) * 4u;
+            const uint32_t rbar = smem_u32(&sm.b.recv_full);
 #pragma unroll
             for (int h4 = 0; h4 < NH; h4 += 4) {
                 const int r = h4 / hs, j0 = h4 - r * hs;
-                st_dsmem4(dsmem_addr(row + (uint32_t)j0 * 4u, (uint32_t)r), __uint_as_float(ov[h4]),
+                st_async4(dsmem_addr(row + (uint32_t)j0 * 4u, (uint32_t)r), __uint_as_float(ov[h4]),
                           __uint_as_float(ov[h4 + 1]), __uint_as_float(ov[h4 + 2]),
-                          __uint_as_float(ov[h4 + 3]));
+                          __uint_as_float(ov[h4 + 3]), dsmem_addr(rbar, (uint32_t)r));
             }
             if (quarter == 0) {  // stats of head h = lane
                 const int r = h / hs, j = h - r * hs;
-                st_dsmem(dsmem_addr(smem_u32(&sm.recv_m[crank][j]), (uint32_t)r), m);
-                st_dsmem(dsmem_addr(smem_u32(&sm.recv_l[crank][j]), (uint32_t)r), l_h);
+                st_async(dsmem_addr(smem_u32(&sm.recv_m[crank][j]), (uint32_t)r), m,
+                         dsmem_addr(rbar, (uint32_t)r));
+                st_async(dsmem_addr(smem_u32(&sm.recv_l[crank][j]), (uint32_t)r), l_h,
+                         dsmem_addr(rbar, (uint32_t)r));
             }
         }
         tc_fence_before();  // the TMEM loads above come before the dealloc below
-        cluster_arrive_release();
-        cluster_wait_acquire();  // every partial of this CTA's heads has arrived
 
         // ---- merge of heads [h0, h0 + hs) from local shared memory
         const int tid = threadIdx.x;
         const int h0 = (int)crank * hs;
+        // every CTA's partial of these heads has landed (a CTA that gave up
+        // sends nothing: the wait then runs out)
+        const bool got = mbar_wait(smem_u32(&sm.b.recv_full), 0, ctx, abort);
         if (tid < hs) {  // per head: the merged max and denominator, each CTA's weight
             const int j = tid;
             const float sink = sm.sink_l2[h0 + j];
@@ -383,32 +397,37 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
                     if (mc != -INFINITY) L += sm.recv_l[c][j] * ex2(mc - mx);
                 }
             }
-            const float inv = L > 0.f ? 1.0f / L : 0.f;
+            const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
             for (int c = 0; c < C; ++c) {
                 const float mc = sm.recv_m[c][j];
                 sm.fac[c][j] = mc != -INFINITY ? ex2(mc - mx) * inv : 0.f;
             }
-            sm.lse_h[j] = L > 0.f ? (mx + log2f(L)) * LN2 : -INFINITY;
+            sm.lse_h[j] = L > 0.f ? (mx + __log2f(L)) * LN2 : -INFINITY;
         }
         softmax_bar();
         // o[h][d] = sum over the cluster's CTAs of fac * O^T[d][h]; d = tid
         const float *rrow = sm.recv + tid * (hs + 4);
         __nv_bfloat16 *ob = p.o + (size_t)bm * NH * HD + tid;
-        for (int j0 = 0; j0 < hs; j0 += 4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int c = 0; c < C; ++c) {
-                const float4 v = *reinterpret_cast<const float4 *>(rrow + c * HD * (hs + 4) + j0);
-                acc.x += sm.fac[c][j0] * v.x;
-                acc.y += sm.fac[c][j0 + 1] * v.y;
-                acc.z += sm.fac[c][j0 + 2] * v.z;
-                acc.w += sm.fac[c][j0 + 3] * v.w;
+        if (got) {
+            for (int j0 = 0; j0 < hs; j0 += 4) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = 0; c < C; ++c) {
+                    const float4 v = *reinterpret_cast<const float4 *>(rrow + c * HD * (hs + 4) + j0);
+                    acc.x += sm.fac[c][j0] * v.x;
+                    acc.y += sm.fac[c][j0 + 1] * v.y;
+                    acc.z += sm.fac[c][j0 + 2] * v.z;
+                    acc.w += sm.fac[c][j0 + 3] * v.w;
+                }
+                ob[(size_t)(h0 + j0) * HD] = __float2bfloat16_rn(acc.x);
+                ob[(size_t)(h0 + j0 + 1) * HD] = __float2bfloat16_rn(acc.y);
+                ob[(size_t)(h0 + j0 + 2) * HD] = __float2bfloat16_rn(acc.z);
+                ob[(size_t)(h0 + j0 + 3) * HD] = __float2bfloat16_rn(acc.w);
             }
-            ob[(size_t)(h0 + j0) * HD] = __float2bfloat16_rn(acc.x);
-            ob[(size_t)(h0 + j0 + 1) * HD] = __float2bfloat16_rn(acc.y);
-            ob[(size_t)(h0 + j0 + 2) * HD] = __float2bfloat16_rn(acc.z);
-            ob[(size_t)(h0 + j0 + 3) * HD] = __float2bfloat16_rn(acc.w);
+            if (tid < hs && p.lse) p.lse[(size_t)bm * NH + h0 + tid] = sm.lse_h[tid];
         }
-        if (tid < hs && p.lse) p.lse[(size_t)bm * NH + h0 + tid] = sm.lse_h[tid];
+        // second cluster phase: this CTA has received everything it expects
+        cluster_arrive_relaxed();
+        cluster_wait_acquire();  // ... and so has every other CTA of the cluster
     }
     if (warp == 0) {
         tc_fence_after();
@@ -445,7 +464,7 @@ cudaError_t launch_sparse_decode(const SparseArgs &a, int C, const DevInfo &dev,
     const size_t smem = sizeof(DecSmem);
     cudaError_t e = ensure_smem_attr((const void *)sparse_decode_kernel, smem, dev);
     if (e != cudaSuccess) return e;
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(a.B * a.M * C));
     cfg.blockDim = dim3(DEC_THREADS);

@@ -520,6 +520,7 @@ __device__ void mma_role(const SpParams &p, SlotSmem &sm, volatile int *abort, u
     uint32_t lastmask = 0;       // bit t & 3: tile t closes its item (known once S(t) issued)
     uint64_t stall_t0 = 0;
     uint32_t spins = 0;
+    if (ctx.stall) mbar_wait(smem_u32(&b.drain), 0, ctx, abort);  // test hook: runs out
     while (pv_item < my_items) {
         bool progress = false;
         if (s_item < my_items) {
@@ -969,7 +970,7 @@ cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream
         cudaError_t e = ensure_smem_attr((const void *)kernel, smem, dev);
         if (e != cudaSuccess) return e;
     }
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     if (verbose())
         fprintf(stderr, "sattn: sparse_tc_kernel<%s> grid=%d block=%d smem=%zu items=%lld splits=%d\n",
                 fp8 ? "fp8" : "bf16", grid, NTHREADS, smem, nitems, splits);

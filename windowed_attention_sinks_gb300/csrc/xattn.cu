@@ -230,6 +230,7 @@ __device__ void mma_issue(const XParams &p, Smem &sm, uint32_t tmem, const DevCt
 }
 
 __device__ void mma_thread(const XParams &p, Smem &sm, uint32_t tmem, const DevCtx &ctx) {
+    if (ctx.stall) mbar_wait(smem_u32(&sm.b.drain), 0, ctx, &sm.abort);  // test hook: runs out
     mma_issue(p, sm, tmem, ctx);
     // every MMA issued completes before TMEM is released (also after an abort)
     tc_commit(smem_u32(&sm.b.drain));
@@ -596,7 +597,7 @@ cudaError_t launch_tc(const XattnArgs &a, const DevInfo &dev, cudaStream_t s) {
         cudaError_t e = ensure_smem_attr((const void *)xattn_tc_kernel<MODE>, smem, dev);
         if (e != cudaSuccess) return e;
     }
-    DevCtx ctx{dev.err, wait_limit_ns()};
+    const DevCtx ctx = make_ctx(dev);
     const int grid = (int)std::min<long long>(items, dev.sm_count > 0 ? dev.sm_count : 1);
     xattn_tc_kernel<MODE><<<grid, NTHREADS, smem, s>>>(tq, tk, p, ctx);
     return cudaGetLastError();
