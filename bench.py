@@ -109,7 +109,7 @@ class ClockSampler:
 # the ncu record behind each workload's roofline.traffic: (kernel, source file);
 # bytes per unit of the workload (query, or compressed row)
 TRAFFIC_RECORD = {
-    "decode": ("sparse_tc_kernel<decode>", "sparse_tc.cu"),
+    "decode": ("sparse_decode_kernel", "sparse_decode.cu"),
     "prefill": ("sparse_tc_kernel<prefill>", "sparse_tc.cu"),
     "decode_fp8": ("sparse_tc_kernel<decode_fp8>", "sparse_tc.cu"),
     "prefill_fp8": ("sparse_tc_kernel<prefill_fp8>", "sparse_tc.cu"),
@@ -451,11 +451,14 @@ def build_path(workload, seed, device, stream):
             launches = 2 if decode else 1
         return Path(
             launch=launch, units=case.B * case.M, nbytes=nbytes,
+            # end to end: a step's queries and index lists come from the host,
+            # its o and lse go back; the cache stays resident
+            e2e_in=[q, idx], e2e_out=[o, lse],
             flops=4 * case.d * valid * case.H,
             # decode is tiny: a scratch buffer larger than L2 is rewritten before each step
             flush=decode, graph=decode, launches=launches, kernel=kernel,
             bound="tensor" if not decode else "hbm",
-            traffic_key=None if (decode and not fp8) else workload,
+            traffic_key=workload,
             name="sparse %s %s: B=%d M=%d H=%d d=%d N=%d K=%d null_logit" % (
                 workload.replace("_fp8", ""),
                 "bf16 q, FP8 cache (e4m3 + row scale, bf16 RoPE half)" if fp8 else "bf16",
@@ -613,6 +616,38 @@ def time_path(p, steps, warmup, stream, world=1, clk=None):
     return cold, warm, graph is not None
 
 
+def time_path_e2e(p, steps, stream):
+    """Queries/s through the public API with host buffers: every step copies
+    its inputs host->device from pinned memory, launches, and reads its
+    outputs back (one stream, synchronised at the end of each step)."""
+    import torch
+
+    hin = [t.cpu().pin_memory() for t in p.e2e_in]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in p.e2e_out]
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for d, h in zip(p.e2e_in, hin):
+                d.copy_(h, non_blocking=True)
+            p.launch(stream)
+            for h, d in zip(hout, p.e2e_out):
+                h.copy_(d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": p.units / dt, "unit": "queries/s", "ms": dt * 1e3,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "schedule": "queries and index lists copied in from pinned host memory, the call, o and "
+                        "lse copied back, one stream, synchronised every step"}
+
+
 def path_record(p, cold, warm, peaks, peaks_src, world, clk_mhz=None, sm_count=152):
     """Median step time, its roofline and the labelled warm-L2 figure."""
     ms = max_over_ranks(float(np.median(cold)), world)
@@ -660,7 +695,10 @@ def run_other(args, rank, world, device, peaks, peaks_src):
     rec = path_record(p, cold, warm, peaks, peaks_src, world, summ.get("sm_mhz"),
                       torch.cuda.get_device_properties(device).multi_processor_count)
     unit_name = "compressed rows" if args.workload == "compress" else "queries"
-    return {
+    e2e = None
+    if getattr(p, "e2e_in", None) and not args.no_e2e:
+        e2e = time_path_e2e(p, max(args.steps, 10), stream)
+    out = {
         "metric": "%s/s (%s)" % (unit_name, args.workload),
         "value": rec["value"],
         "unit": "%s/s" % unit_name, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -679,6 +717,9 @@ def run_other(args, rank, world, device, peaks, peaks_src):
         "gpu_launches": args.steps * p.launches,
         "clocks": summ,
     }
+    if e2e is not None:
+        out["e2e"] = e2e
+    return out
 
 
 def measure_paths(names, rank, world, device, peaks, peaks_src, steps=50, warmup=5):
@@ -695,6 +736,8 @@ def measure_paths(names, rank, world, device, peaks, peaks_src, steps=50, warmup
         rec = path_record(p, cold, warm, peaks, peaks_src, world, None, sms)
         rec["workload"] = p.name
         rec["launch"] = "CUDA graph replay, L2 flushed" if graphed else "direct"
+        if getattr(p, "e2e_in", None):
+            rec["e2e"] = time_path_e2e(p, steps, stream)
         out[name] = rec
         del p
         torch.cuda.empty_cache()

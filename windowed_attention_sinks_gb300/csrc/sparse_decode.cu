@@ -52,7 +52,8 @@ constexpr int RECV_FLOATS = MAX_CLUSTER * HD * (NH / MAX_CLUSTER + 4);
 
 struct DecBars {
     uint64_t q_full;
-    uint64_t kv_full[DT_MAX], s_full[DT_MAX], p_full[DT_MAX];
+    uint64_t kv_full[DT_MAX], s_full[DT_MAX];
+    uint64_t p_full;     // P of every tile written (each softmax warp arrives once)
     uint64_t o_full, drain;
     uint64_t recv_full;  // every CTA's partial of this CTA's heads has landed (tx bytes)
 };
@@ -118,9 +119,11 @@ __device__ void dec_mma(const DecSmem &sm, DecBars &b, uint32_t tmem, int nt, vo
         tc_commit(smem_u32(&b.s_full[t]));
         ++issued;
     }
+    // P of all tiles is written together: one wait, then every P V back to
+    // back (a barrier access of this thread stalls the MMAs already queued)
+    if (ok && issued > 0) ok = mbar_wait(smem_u32(&b.p_full), 0, ctx, abort);
+    if (ok) tc_fence_after();
     for (int t = 0; ok && t < issued; ++t) {
-        if (!(ok = mbar_wait(smem_u32(&b.p_full[t]), 0, ctx, abort))) break;
-        tc_fence_after();
         const uint64_t a = desc_sw128(smem_u32(sm.kv[t]), KV_HALF);
         const uint64_t bp = desc_sw128(smem_u32(sm.p[t]), 16u);
 #pragma unroll
@@ -178,8 +181,8 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
         for (int t = 0; t < DT_MAX; ++t) {
             mbar_init(smem_u32(&b.kv_full[t]), 32 * COPY_WARPS);
             mbar_init(smem_u32(&b.s_full[t]), 1);
-            mbar_init(smem_u32(&b.p_full[t]), 4);
         }
+        mbar_init(smem_u32(&b.p_full), 4);
         mbar_init(smem_u32(&b.o_full), 1);
         mbar_init(smem_u32(&b.drain), 1);
         mbar_init(smem_u32(&b.recv_full), 1);
@@ -327,8 +330,7 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
             fence_proxy_async_smem();  // P is read by the tensor core
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                for (int t = 0; t < nt; ++t) mbar_arrive(smem_u32(&sm.b.p_full[t]));
+            if (lane == 0) mbar_arrive(smem_u32(&sm.b.p_full));
         }
         {
             float a0, a1;
