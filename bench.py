@@ -111,7 +111,7 @@ class ClockSampler:
 TRAFFIC_RECORD = {
     "decode": ("sparse_decode_kernel", "sparse_decode.cu"),
     "prefill": ("sparse_tc_kernel<prefill>", "sparse_tc.cu"),
-    "decode_fp8": ("sparse_tc_kernel<decode_fp8>", "sparse_tc.cu"),
+    "decode_fp8": ("sparse_decode_kernel<fp8>", "sparse_decode.cu"),
     "prefill_fp8": ("sparse_tc_kernel<prefill_fp8>", "sparse_tc.cu"),
     "block": ("attn_tc_kernel<block>", "attn_tc.cu"),
     "select": ("xattn_tc_kernel<1>", "xattn.cu"),
@@ -441,14 +441,12 @@ def build_path(workload, seed, device, stream):
             else:
                 sa.sparse_fwd(q, kv, idx, sinks, case.sink_mode, case.scale, o=o, lse=lse,
                               workspace=ws, stream=st or stream)
-        # launches per step: the cluster kernel alone for bf16 decode (its
-        # splits merge on chip), else the persistent kernel plus the merge
-        # when it splits lists
-        if decode and not fp8:
-            kernel, launches = "sparse_decode_kernel", 1
+        # launches per step: the cluster kernel alone for decode (its splits
+        # merge on chip), the persistent kernel for prefill
+        if decode:
+            kernel, launches = "sparse_decode_kernel" + ("<fp8>" if fp8 else ""), 1
         else:
-            kernel = "sparse_tc_kernel<%s>" % workload
-            launches = 2 if decode else 1
+            kernel, launches = "sparse_tc_kernel<%s>" % workload, 1
         return Path(
             launch=launch, units=case.B * case.M, nbytes=nbytes,
             # end to end: a step's queries and index lists come from the host,

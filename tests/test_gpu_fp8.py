@@ -131,6 +131,30 @@ def test_matches_bf16_path_on_exact_rows():
     assert torch.equal(o8, o16) and torch.equal(l8, l16)
 
 
+def test_cluster_path_matches_bf16_on_exact_rows():
+    # 16 queries take the cluster kernel with either cache; on rows that
+    # dequantise to themselves the two calls sum the same values in the same
+    # order, so the results agree bit for bit
+    case = W.sparse_decode_bf16(8, B=16)
+    rng = np.random.default_rng(8)
+    vals = oracle.e4m3_decode(rng.integers(0, 0x7F, case.kv.shape[:2] + (64,)).astype(np.uint8))
+    sign = np.where(rng.random(vals.shape) < 0.5, -1.0, 1.0)
+    case.kv[..., :64] = (vals * sign / 64.0).astype(np.float32)
+    case.kv[..., 0] = 7.0
+    codes, rope, scale, deq = _fp8_cache(case)
+    assert np.array_equal(deq, case.kv)
+    for mode in (0, 1, 2):
+        o8, l8 = run_fp8(case, codes, rope, scale, mode=mode, workspace=False)
+        q, kv = dev(case.q, torch.bfloat16), dev(case.kv, torch.bfloat16)
+        idx = dev(case.idx, torch.int32)
+        s16 = dev(case.sinks, torch.float32) if mode else None
+        o16, l16 = sa.sparse_fwd(q, kv, idx, s16, mode, case.scale)
+        sa.check_device()
+        assert torch.equal(o8, o16) and torch.equal(l8, l16), mode
+        ro, rl = oracle.sparse(case.q, deq, case.idx, case.sinks, mode, case.scale)
+        compare(o8, l8, ro, rl, TOL_BF16_O, what="fp8 cluster mode=%d" % mode)
+
+
 def test_lists_of_only_invalid_entries():
     # every entry -1: o = 0 and lse = the sink (null logit) for every head
     case = W.sparse_decode_bf16(7, B=3)

@@ -71,8 +71,9 @@ def _sparse(B):
     return call, ref
 
 
-def _sparse_fp8():
-    case = W.sparse_decode_bf16(5, B=4)
+def _sparse_fp8(B):
+    # B = 4: the cluster kernel; B = 100: the persistent kernel with split lists
+    case = W.sparse_decode_bf16(5, B=B)
     q, idx = dev(case.q, torch.bfloat16), dev(case.idx, torch.int32)
     s = dev(case.sinks, torch.float32)
     nope, rope, scl = sa.quantize_kv_fp8(dev(case.kv, torch.bfloat16), case.d // 2)
@@ -81,8 +82,12 @@ def _sparse_fp8():
     deq = oracle.bf16_round(oracle.dequantize_kv_fp8(
         nope.cpu().numpy(), rope.float().cpu().numpy(), scl.cpu().numpy()).astype(np.float32))
 
+    ws = torch.empty(max(1, sa.sparse_workspace_bytes(case.B, case.M, case.H, case.d, case.K)),
+                     dtype=torch.uint8, device="cuda")
+
     def call():
-        return sa.sparse_fp8_fwd(q, nope, rope, scl, idx, s, case.sink_mode, case.scale)
+        return sa.sparse_fp8_fwd(q, nope, rope, scl, idx, s, case.sink_mode, case.scale,
+                                 workspace=ws)
 
     def ref():
         return oracle.sparse(case.q, deq, case.idx, case.sinks, case.sink_mode, case.scale)
@@ -105,7 +110,8 @@ def _xattn():
 
 
 FAMILIES = {"window": _window, "block": _block, "sparse_cluster": lambda: _sparse(4),
-            "sparse_persistent": lambda: _sparse(100), "sparse_fp8": _sparse_fp8,
+            "sparse_persistent": lambda: _sparse(100), "sparse_fp8_cluster": lambda: _sparse_fp8(4),
+            "sparse_fp8_persistent": lambda: _sparse_fp8(100),
             "xattn_stats": _xattn}
 
 

@@ -150,7 +150,7 @@ cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t
 cudaError_t launch_sparse_tc(const SparseArgs &a, const DevInfo &dev, cudaStream_t s);
 // Few queries: each query's list cut into C segments, one per CTA of a
 // cluster, merged through distributed shared memory. Returns the cluster
-// size C for a shape this kernel takes (bf16, H = 32, d = 128), else 0.
+// size C for a shape this kernel takes (H = 32, d = 128; bf16 or FP8 cache), else 0.
 int sparse_decode_cluster(int B, int M, int K, int sm_count);
 cudaError_t launch_sparse_decode(const SparseArgs &a, int C, const DevInfo &dev, cudaStream_t s);
 size_t sparse_tc_workspace_bytes(int B, int M, int H, int d, int K);

@@ -18,16 +18,21 @@
 //     P (bf16) and the row sums, no rescaling,
 //   - accumulates O^T += KV^T P^T over the tiles,
 //   - leaves its partial (m, l, O^T) in shared memory.
-// CTA r of the cluster owns heads [r 32/C, (r+1) 32/C) of the query: every
-// CTA sends its partial of those heads (O^T rows, m, l) straight into CTA
-// r's shared memory with asynchronous stores whose bytes complete on CTA
-// r's own mbarrier, so a CTA starts merging as soon as its heads' partials
-// have landed. It merges them through the log-sum-exp (the null-logit sink
-// is added here, once) and writes o and lse. One launch, no workspace.
+// The merge through the log-sum-exp is split in two exchanges, both
+// asynchronous stores into the other CTAs' shared memory whose bytes
+// complete on the receiver's own mbarrier. As soon as its P is written each
+// CTA sends its (m, l) of all 32 heads to every CTA of the cluster; while P V
+// runs, every CTA computes each head's merged max and denominator (the
+// null-logit sink added here, once), lse and its own weight. CTA r owns heads
+// [r 32/C, (r+1) 32/C) of the query: every CTA scales its O^T rows of those
+// heads by its weight and sends them to CTA r, which adds what it receives
+// and writes o and lse. One launch, no workspace.
 //
 // Warps 0-3: Q copy, softmax, epilogue and merge (warp w reads TMEM lanes
 // 32w .. 32w+31); warps 4-7: row copies (warp 4 + g: rows 32g .. 32g+31 of
-// each tile), after which lane 0 of warp 4 issues the MMAs.
+// each tile), after which lane 0 of warp 4 issues the MMAs. With an FP8
+// cache the copy warps take the bf16 RoPE half by cp.async and dequantise the
+// e4m3 half into the stage (Fp8Copier); everything else is the same.
 #include <math.h>
 #include <stdio.h>
 
@@ -55,26 +60,28 @@ struct DecBars {
     uint64_t kv_full[DT_MAX], s_full[DT_MAX];
     uint64_t p_full;     // P of every tile written (each softmax warp arrives once)
     uint64_t o_full, drain;
-    uint64_t recv_full;  // every CTA's partial of this CTA's heads has landed (tx bytes)
+    uint64_t stats_full; // every CTA's (m, l) of all heads has landed (tx bytes)
+    uint64_t recv_full;  // every CTA's weighted O^T rows of this CTA's heads (tx bytes)
 };
 
-// Bytes a CTA receives: from each of the C CTAs, HD rows of hs = NH / C O^T
-// values and hs (m, l) pairs; C hs = NH.
-constexpr uint32_t RECV_BYTES = NH * (HD * 4 + 8);
+// Bytes a CTA receives: (m, l) of all NH heads from each of the C CTAs; and
+// from each of them HD rows of hs = NH / C weighted O^T values (C hs = NH).
+constexpr uint32_t STATS_BYTES_PER_CTA = NH * 8;
+constexpr uint32_t RECV_BYTES = NH * HD * 4;
 
 struct alignas(1024) DecSmem {
     uint8_t kv[DT_MAX][KV_TILE];
     uint8_t q[2 * QP_HALF];
     uint8_t p[DT_MAX][2 * QP_HALF];
     float tbuf[4][NH * TB_STRIDE];
-    // partials of this CTA's heads pushed by every CTA c of the cluster:
-    // O^T rows recv[(c HD + d) (hs + 4) + j] (unnormalised), and the stats
-    // (log2 units) of head j
+    // weighted O^T rows of this CTA's heads sent by every CTA c of the
+    // cluster: recv[(c HD + d) (hs + 4) + j]
     float recv[RECV_FLOATS];
-    float recv_m[MAX_CLUSTER][NH], recv_l[MAX_CLUSTER][NH];
-    float fac[MAX_CLUSTER][NH];         // merge weight of each CTA's partial per head
+    float stat_m[MAX_CLUSTER][NH], stat_l[MAX_CLUSTER][NH];  // every CTA's (m, l), log2 units
+    float wself[NH];                    // this CTA's weight per head in the merged result
     float lse_h[NH];
     float sink_l2[NH];                  // null-logit sinks x log2(e), -inf without
+    int ids[DT_MAX][R];                 // FP8: each tile's entries, read by the copier
     float xmax[4][NH];                  // per-warp maxima of the segment
     float lpart[4][NH];                 // per-warp row sums
     DecBars b;
@@ -86,6 +93,11 @@ static_assert(sizeof(DecSmem) <= 227 * 1024, "shared memory of one CTA");
 
 struct DecParams {
     const __nv_bfloat16 *q, *kv;
+    // FP8 cache: e4m3 codes of the first DN columns, one scale per row, bf16
+    // RoPE part (the last HD - DN columns)
+    const uint8_t *kv_nope;
+    const __nv_bfloat16 *kv_rope;
+    const float *kv_scale;
     const int32_t *idx;
     const float *sinks;
     int sink_mode;
@@ -138,6 +150,7 @@ __device__ void dec_mma(const DecSmem &sm, DecBars &b, uint32_t tmem, int nt, vo
     mbar_wait(smem_u32(&b.drain), 0, ctx, &zero);
 }
 
+template <bool FP8>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
 sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
     extern __shared__ __align__(1024) uint8_t dsmem[];
@@ -179,12 +192,15 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
         DecBars &b = sm.b;
         mbar_init(smem_u32(&b.q_full), 128);
         for (int t = 0; t < DT_MAX; ++t) {
-            mbar_init(smem_u32(&b.kv_full[t]), 32 * COPY_WARPS);
+            // FP8: each copy warp also arrives once after its dequantised stores
+            mbar_init(smem_u32(&b.kv_full[t]), 32 * COPY_WARPS + (FP8 ? COPY_WARPS : 0));
             mbar_init(smem_u32(&b.s_full[t]), 1);
         }
         mbar_init(smem_u32(&b.p_full), 4);
         mbar_init(smem_u32(&b.o_full), 1);
         mbar_init(smem_u32(&b.drain), 1);
+        mbar_init(smem_u32(&b.stats_full), 1);
+        mbar_arrive_expect_tx(smem_u32(&b.stats_full), STATS_BYTES_PER_CTA * (uint32_t)p.C);
         mbar_init(smem_u32(&b.recv_full), 1);
         mbar_arrive_expect_tx(smem_u32(&b.recv_full), RECV_BYTES);
         sm.abort = 0;
@@ -216,13 +232,46 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
     if (warp >= 4) {
         // ---- row copies: all tiles at once
         const int g = warp - 4;
-        const RowCopier cp(lane);
-        const __nv_bfloat16 *rows = p.kv + (size_t)(bm / p.M) * p.N * HD;
+        const size_t row0 = (size_t)(bm / p.M) * p.N;  // first cache row of the request
+        if (!FP8) {
+            const RowCopier cp(lane);
+            const __nv_bfloat16 *rows = p.kv + row0 * HD;
 #pragma unroll
-        for (int t = 0; t < DT_MAX; ++t) {
-            if (t < nt) {
-                cp.issue_lanes(smem_u32(sm.kv[t]), e[t], rows, g);
-                cp_async_arrive(smem_u32(&sm.b.kv_full[t]));
+            for (int t = 0; t < DT_MAX; ++t) {
+                if (t < nt) {
+                    cp.issue_lanes(smem_u32(sm.kv[t]), e[t], rows, g);
+                    cp_async_arrive(smem_u32(&sm.b.kv_full[t]));
+                }
+            }
+        } else {
+            const Fp8Copier fc(lane);
+            // the copier reads each tile's entries by row
+#pragma unroll
+            for (int t = 0; t < DT_MAX; ++t)
+                if (t < nt) sm.ids[t][32 * g + lane] = e[t];
+            __syncwarp();
+            uint4 codes[DT_MAX][4];
+            float scl[DT_MAX][4];
+#pragma unroll
+            for (int t = 0; t < DT_MAX; ++t)
+                if (t < nt)
+                    fc.load_codes(sm.ids[t], p.kv_nope + row0 * DN, p.kv_scale + row0, g, codes[t],
+                                  scl[t]);
+#pragma unroll
+            for (int t = 0; t < DT_MAX; ++t) {
+                if (t < nt) {
+                    fc.issue_rope(smem_u32(sm.kv[t]), sm.ids[t], p.kv_rope + row0 * (HD - DN), g);
+                    cp_async_arrive(smem_u32(&sm.b.kv_full[t]));
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < DT_MAX; ++t) {
+                if (t < nt) {
+                    fc.store_codes(smem_u32(sm.kv[t]), g, codes[t], scl[t]);
+                    fence_proxy_async_smem();  // the stores are read by the tensor core
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sm.b.kv_full[t]));
+                }
             }
         }
         if (warp == 4) {
@@ -337,13 +386,44 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
             f2_unpack(f2_add(ls2a, ls2b), a0, a1);
             sm.lpart[quarter][h] = a0 + a1;
         }
+        softmax_bar();  // lpart complete
+        const float l_h = (sm.lpart[0][h] + sm.lpart[1][h]) + (sm.lpart[2][h] + sm.lpart[3][h]);
+        const int hs = NH / C;
+        // ---- (m, l) of every head to every CTA of the cluster, while P V runs
+        cluster_wait_acquire();  // every CTA of the cluster is running, its barriers set up
+        if (quarter == 0) {  // head h = lane
+            const uint32_t am = smem_u32(&sm.stat_m[crank][h]), al = smem_u32(&sm.stat_l[crank][h]);
+            const uint32_t sbar = smem_u32(&sm.b.stats_full);
+            for (int r = 0; r < C; ++r) {
+                st_async(dsmem_addr(am, (uint32_t)r), m, dsmem_addr(sbar, (uint32_t)r));
+                st_async(dsmem_addr(al, (uint32_t)r), l_h, dsmem_addr(sbar, (uint32_t)r));
+            }
+        }
+        // merged max and denominator per head (null-logit sink added once),
+        // lse, and this CTA's weight; a CTA that gave up sends nothing and the
+        // wait then runs out
+        const bool got_stats = mbar_wait(smem_u32(&sm.b.stats_full), 0, ctx, abort);
+        if (quarter == 0) {
+            const float sink = sm.sink_l2[h];
+            float mx = sink;
+            for (int c = 0; c < C; ++c) mx = fmaxf(mx, sm.stat_m[c][h]);
+            float L = 0.f;
+            if (mx != -INFINITY && got_stats) {
+                L = ex2(sink - mx);  // 0 without a null-logit sink
+                for (int c = 0; c < C; ++c) {
+                    const float mc = sm.stat_m[c][h];
+                    if (mc != -INFINITY) L += sm.stat_l[c][h] * ex2(mc - mx);
+                }
+            }
+            sm.wself[h] = (m != -INFINITY && L > 0.f) ? ex2(m - mx) * __frcp_rn(L) : 0.f;
+            sm.lse_h[h] = L > 0.f ? (mx + __log2f(L)) * LN2 : -INFINITY;
+        }
         if (nt > 0) {
             if (!failed) failed = !mbar_wait(smem_u32(&sm.b.o_full), 0, ctx, abort);
             failed = __any_sync(0xffffffffu, failed);
         }
-        softmax_bar();  // lpart complete
-        const float l_h = (sm.lpart[0][h] + sm.lpart[1][h]) + (sm.lpart[2][h] + sm.lpart[3][h]);
-        // O^T row d = 32 quarter + lane: 32 heads
+        softmax_bar();  // wself complete
+        // O^T row d = 32 quarter + lane: 32 heads, times this CTA's weights
         uint32_t ov[32];
         if (nt > 0 && !failed) {
             tc_fence_after();
@@ -353,11 +433,18 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
 #pragma unroll
             for (int hh = 0; hh < 32; ++hh) ov[hh] = 0u;  // nothing seen: a zero partial
         }
+        tc_fence_before();  // the TMEM loads above come before the dealloc below
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float4 w = *reinterpret_cast<const float4 *>(&sm.wself[4 * k]);
+            ov[4 * k] = __float_as_uint(__uint_as_float(ov[4 * k]) * w.x);
+            ov[4 * k + 1] = __float_as_uint(__uint_as_float(ov[4 * k + 1]) * w.y);
+            ov[4 * k + 2] = __float_as_uint(__uint_as_float(ov[4 * k + 2]) * w.z);
+            ov[4 * k + 3] = __float_as_uint(__uint_as_float(ov[4 * k + 3]) * w.w);
+        }
         // the Q copies have landed (a CTA without tiles never waited for them)
         asm volatile("cp.async.wait_all;" ::: "memory");
-        // ---- send: heads of CTA r go to CTA r's shared memory
-        const int hs = NH / C;
-        cluster_wait_acquire();  // every CTA of the cluster is running, its barriers set up
+        // ---- weighted O^T rows: heads of CTA r go to CTA r's shared memory
         {
             const int d = quarter * 32 + lane;
             const uint32_t row = smem_u32(sm.recv) +
@@ -370,44 +457,12 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
                           __uint_as_float(ov[h4 + 1]), __uint_as_float(ov[h4 + 2]),
                           __uint_as_float(ov[h4 + 3]), dsmem_addr(rbar, (uint32_t)r));
             }
-            if (quarter == 0) {  // stats of head h = lane
-                const int r = h / hs, j = h - r * hs;
-                st_async(dsmem_addr(smem_u32(&sm.recv_m[crank][j]), (uint32_t)r), m,
-                         dsmem_addr(rbar, (uint32_t)r));
-                st_async(dsmem_addr(smem_u32(&sm.recv_l[crank][j]), (uint32_t)r), l_h,
-                         dsmem_addr(rbar, (uint32_t)r));
-            }
         }
-        tc_fence_before();  // the TMEM loads above come before the dealloc below
 
-        // ---- merge of heads [h0, h0 + hs) from local shared memory
+        // ---- o of heads [h0, h0 + hs): the sum of what the cluster sent
         const int tid = threadIdx.x;
         const int h0 = (int)crank * hs;
-        // every CTA's partial of these heads has landed (a CTA that gave up
-        // sends nothing: the wait then runs out)
         const bool got = mbar_wait(smem_u32(&sm.b.recv_full), 0, ctx, abort);
-        if (tid < hs) {  // per head: the merged max and denominator, each CTA's weight
-            const int j = tid;
-            const float sink = sm.sink_l2[h0 + j];
-            float mx = sink;
-            for (int c = 0; c < C; ++c) mx = fmaxf(mx, sm.recv_m[c][j]);
-            float L = 0.f;
-            if (mx != -INFINITY) {
-                L = ex2(sink - mx);  // 0 without a null-logit sink
-                for (int c = 0; c < C; ++c) {
-                    const float mc = sm.recv_m[c][j];
-                    if (mc != -INFINITY) L += sm.recv_l[c][j] * ex2(mc - mx);
-                }
-            }
-            const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
-            for (int c = 0; c < C; ++c) {
-                const float mc = sm.recv_m[c][j];
-                sm.fac[c][j] = mc != -INFINITY ? ex2(mc - mx) * inv : 0.f;
-            }
-            sm.lse_h[j] = L > 0.f ? (mx + __log2f(L)) * LN2 : -INFINITY;
-        }
-        softmax_bar();
-        // o[h][d] = sum over the cluster's CTAs of fac * O^T[d][h]; d = tid
         const float *rrow = sm.recv + tid * (hs + 4);
         __nv_bfloat16 *ob = p.o + (size_t)bm * NH * HD + tid;
         if (got) {
@@ -415,17 +470,17 @@ sparse_decode_kernel(const DecParams p, const DevCtx ctx) {
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int c = 0; c < C; ++c) {
                     const float4 v = *reinterpret_cast<const float4 *>(rrow + c * HD * (hs + 4) + j0);
-                    acc.x += sm.fac[c][j0] * v.x;
-                    acc.y += sm.fac[c][j0 + 1] * v.y;
-                    acc.z += sm.fac[c][j0 + 2] * v.z;
-                    acc.w += sm.fac[c][j0 + 3] * v.w;
+                    acc.x += v.x;
+                    acc.y += v.y;
+                    acc.z += v.z;
+                    acc.w += v.w;
                 }
                 ob[(size_t)(h0 + j0) * HD] = __float2bfloat16_rn(acc.x);
                 ob[(size_t)(h0 + j0 + 1) * HD] = __float2bfloat16_rn(acc.y);
                 ob[(size_t)(h0 + j0 + 2) * HD] = __float2bfloat16_rn(acc.z);
                 ob[(size_t)(h0 + j0 + 3) * HD] = __float2bfloat16_rn(acc.w);
             }
-            if (tid < hs && p.lse) p.lse[(size_t)bm * NH + h0 + tid] = sm.lse_h[tid];
+            if (tid < hs && p.lse) p.lse[(size_t)bm * NH + h0 + tid] = sm.lse_h[h0 + tid];
         }
         // second cluster phase: this CTA has received everything it expects
         cluster_arrive_relaxed();
@@ -449,9 +504,13 @@ int sparse_decode_cluster(int B, int M, int K, int sm_count) {
 }
 
 cudaError_t launch_sparse_decode(const SparseArgs &a, int C, const DevInfo &dev, cudaStream_t s) {
+    const bool fp8 = a.kv == nullptr;
     DecParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.kv = static_cast<const __nv_bfloat16 *>(a.kv);
+    p.kv_nope = a.kv_nope;
+    p.kv_rope = static_cast<const __nv_bfloat16 *>(a.kv_rope);
+    p.kv_scale = a.kv_scale;
     p.idx = a.idx;
     p.sinks = a.sinks;
     p.sink_mode = a.sink_mode;
@@ -464,7 +523,8 @@ cudaError_t launch_sparse_decode(const SparseArgs &a, int C, const DevInfo &dev,
     p.C = C;
     p.seg = (a.K + C - 1) / C;
     const size_t smem = sizeof(DecSmem);
-    cudaError_t e = ensure_smem_attr((const void *)sparse_decode_kernel, smem, dev);
+    auto kernel = fp8 ? sparse_decode_kernel<true> : sparse_decode_kernel<false>;
+    cudaError_t e = ensure_smem_attr((const void *)kernel, smem, dev);
     if (e != cudaSuccess) return e;
     const DevCtx ctx = make_ctx(dev);
     cudaLaunchConfig_t cfg{};
@@ -480,9 +540,9 @@ cudaError_t launch_sparse_decode(const SparseArgs &a, int C, const DevInfo &dev,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (verbose())
-        fprintf(stderr, "sattn: sparse_decode_kernel grid=%d cluster=%d block=%d smem=%zu seg=%d\n",
-                a.B * a.M * C, C, DEC_THREADS, smem, p.seg);
-    return cudaLaunchKernelEx(&cfg, sparse_decode_kernel, p, ctx);
+        fprintf(stderr, "sattn: sparse_decode_kernel<%s> grid=%d cluster=%d block=%d smem=%zu seg=%d\n",
+                fp8 ? "fp8" : "bf16", a.B * a.M * C, C, DEC_THREADS, smem, p.seg);
+    return cudaLaunchKernelEx(&cfg, kernel, p, ctx);
 }
 
 }  // namespace sattn

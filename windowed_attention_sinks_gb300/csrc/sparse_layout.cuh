@@ -13,6 +13,8 @@
 // QP_HALF bytes each, 128B-swizzled.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 
 namespace sattn {
@@ -97,6 +99,86 @@ struct RowCopier {
             const int e = __shfl_sync(0xffffffffu, e_lane, 2 * i2 + hi);
             cp_async16(kv_s + dofs[i2 & 3] + (uint32_t)i * 256u,
                        src0 + (size_t)(e >= 0 ? e : 0) * HD, e >= 0 ? 16u : 0u);
+        }
+    }
+};
+
+// FP8 cache rows: the RoPE part (bf16, the stage's second 64-column half) is
+// copied by cp.async like the bf16 rows; the DN e4m3 codes are loaded to
+// registers before the stage is free, then dequantised (code value x row
+// scale, rounded to bf16) and stored into the first half with the same 128B
+// swizzle.
+constexpr int DN = HD / 2;  // non-RoPE columns
+
+struct Fp8Copier {
+    uint32_t rope_dofs[2];
+    int rsub, ru, rn, cu;
+    // RoPE: lane = (rsub, ru) copies unit ru of rows 4k + rsub (four rows per
+    // instruction); codes: lane = (rn, cu) handles codes 16 cu .. 16 cu + 15 of
+    // rows 8k + rn. A warp's rows start at a multiple of 8, so the swizzle
+    // term of row 4k + rsub is rsub | 4 (k & 1), that of row 8k + rn is rn.
+    __device__ explicit Fp8Copier(int lane) {
+        rsub = lane >> 3;
+        ru = lane & 7;
+        rn = lane >> 2;
+        cu = lane & 3;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            rope_dofs[j] = KV_HALF + (uint32_t)rsub * 128u +
+                           (((uint32_t)ru ^ ((uint32_t)rsub | (4u * j))) << 4);
+    }
+    // codes and scales of this warp's rows (32 g .. 32 g + 31) to registers
+    __device__ void load_codes(const int *ids, const uint8_t *nope, const float *scl, int g,
+                               uint4 (&q)[4], float (&sc)[4]) const {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int e = ids[32 * g + 8 * k + rn];
+            if (e >= 0) {
+                q[k] = __ldg(reinterpret_cast<const uint4 *>(nope + (size_t)e * DN) + cu);
+                sc[k] = __ldg(scl + e);
+            } else {  // -1 entry: a zero row keeps P V finite
+                q[k] = make_uint4(0u, 0u, 0u, 0u);
+                sc[k] = 0.f;
+            }
+        }
+    }
+    __device__ void issue_rope(uint32_t kv_s, const int *ids, const __nv_bfloat16 *rope,
+                               int g) const {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int e = ids[32 * g + 4 * k + rsub];
+            cp_async16(kv_s + (uint32_t)(32 * g + 4 * k) * 128u + rope_dofs[k & 1],
+                       rope + (size_t)(e >= 0 ? e : 0) * (HD - DN) + ru * 8, e >= 0 ? 16u : 0u);
+        }
+    }
+    // codes -> bf16 (e4m3 value x scale, rounded to nearest even) into the
+    // stage's first half
+    __device__ void store_codes(uint32_t kv_s, int g, const uint4 (&q)[4],
+                                const float (&sc)[4]) const {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const __nv_fp8x2_storage_t two =
+                        (__nv_fp8x2_storage_t)((w[i] >> (16 * hh)) & 0xffffu);
+                    const __half2 h2 = __half2(__nv_cvt_fp8x2_to_halfraw2(two, __NV_E4M3));
+                    const float2 f = __half22float2(h2);
+                    o[2 * i + hh] = pack_bf16x2(f.x * sc[k], f.y * sc[k]);
+                }
+            }
+            const uint32_t row = kv_s + (uint32_t)(32 * g + 8 * k + rn) * 128u;
+            const uint32_t a0 = row + ((((uint32_t)(2 * cu)) ^ (uint32_t)rn) << 4);
+            const uint32_t a1 = row + ((((uint32_t)(2 * cu + 1)) ^ (uint32_t)rn) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a0), "r"(o[0]),
+                         "r"(o[1]), "r"(o[2]), "r"(o[3])
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a1), "r"(o[4]),
+                         "r"(o[5]), "r"(o[6]), "r"(o[7])
+                         : "memory");
         }
     }
 };
