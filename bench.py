@@ -610,6 +610,18 @@ def time_path(p, steps, warmup, stream, world=1, clk=None):
     else:
         cold = run(steps, True)
     warm = run(max(steps, 20), False)
+    if graph is not None:
+        # 100 replays back to back between two events: launches pipeline
+        # behind each other, which exposes what one launch costs in a stream
+        # of them
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(100):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        p.back_to_back_ms = e0.elapsed_time(e1) / 100
     sa.check_device(stream)
     return cold, warm, graph is not None
 
@@ -675,10 +687,13 @@ def path_record(p, cold, warm, peaks, peaks_src, world, clk_mhz=None, sm_count=1
     roof["peak_source"] = peaks_src
     roof["tflops"] = tf
     roof["tensor_frac"] = tf / peaks.get("bf16_tflops_sustained", 1700.0)
-    return {"ms": ms, "ms_mean": float(np.mean(cold)), "runs": len(cold),
-            "value": whole_job_rate(p.units, world, ms), "unit": "queries/s",
-            "warm_l2_ms": ms_warm, "launches_per_step": p.launches, "kernel": p.kernel,
-            "roofline": roof}
+    rec = {"ms": ms, "ms_mean": float(np.mean(cold)), "runs": len(cold),
+           "value": whole_job_rate(p.units, world, ms), "unit": "queries/s",
+           "warm_l2_ms": ms_warm, "launches_per_step": p.launches, "kernel": p.kernel,
+           "roofline": roof}
+    if getattr(p, "back_to_back_ms", None) is not None:
+        rec["back_to_back_ms"] = p.back_to_back_ms
+    return rec
 
 
 def run_other(args, rank, world, device, peaks, peaks_src):
@@ -712,6 +727,7 @@ def run_other(args, rank, world, device, peaks, peaks_src):
                              "steps back to back, no flush" % args.steps},
         "roofline": rec["roofline"],
         "ms_mean": rec["ms_mean"], "warm_l2_ms": rec["warm_l2_ms"],
+        "back_to_back_ms": rec.get("back_to_back_ms"),
         "gpu_launches": args.steps * p.launches,
         "clocks": summ,
     }
