@@ -119,19 +119,29 @@ TRAFFIC_RECORD = {
 }
 
 
+def code_sha256(path):
+    """sha256 of a C/C++/CUDA source with its comments and whitespace removed:
+    it changes when the code changes, not when a comment does."""
+    import hashlib
+    import re
+
+    with open(path) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return hashlib.sha256("".join(src.split()).encode()).hexdigest()
+
+
 def profiled_traffic(kernel, source_name, units):
     """DRAM bytes per launch from the committed ncu record, scaled to `units`
-    query tokens; None when the kernel source changed since the capture."""
-    import hashlib
-
+    query tokens; None when the kernel's code changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[kernel]
-        with open(os.path.join(ROOT, "windowed_attention_sinks_gb300", "csrc", source_name), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        sha = code_sha256(os.path.join(ROOT, "windowed_attention_sinks_gb300", "csrc", source_name))
     except (OSError, KeyError, ValueError):
         return None
-    if sha != rec.get("source_sha256"):
+    if sha != rec.get("code_sha256"):
         return None
     return rec["bytes_per_query_token"] * units
 

@@ -17,7 +17,7 @@
 //   - takes the softmax over the whole segment: the segment's max first, then
 //     P (bf16) and the row sums, no rescaling,
 //   - accumulates O^T += KV^T P^T over the tiles,
-//   - leaves its partial (m, l, O^T) in shared memory.
+//   - takes part in the merge of the cluster's partials (m, l, O^T).
 // The merge through the log-sum-exp is split in two exchanges, both
 // asynchronous stores into the other CTAs' shared memory whose bytes
 // complete on the receiver's own mbarrier. As soon as its P is written each
