@@ -113,9 +113,16 @@ sattn_status sattn_window_fwd(const void *q, const void *k, const void *v, void 
  *   o [B, M, H, d] (dtype), lse [B, M, H] float32 or NULL.
  *   workspace: NULL or a caller-owned device buffer of at least
  *     sattn_sparse_workspace_bytes(B, M, H, d, K) bytes, 256-byte aligned.
- *     With a workspace the index list may be split across CTAs and the
- *     partial results merged through their LSE on the device; without one
- *     each query's list is processed by a single CTA.
+ * Execution (bf16, H == 32, d == 128): with at most as many queries (B M) as
+ *   the device has SMs, and lists short enough for eight CTAs of 384 entries,
+ *   each query's list is cut into segments handled by the CTAs of one
+ *   thread-block cluster, whose partials merge through their LSE in shared
+ *   memory, in one launch; the workspace is not used. Otherwise a persistent
+ *   kernel runs: with a workspace it may split each list across CTAs and
+ *   merge the partial results in a second launch; without one each query's
+ *   list is processed by a single CTA. Every path gives the same result up to
+ *   floating-point summation order. F32 (and bf16 with other H) runs one warp
+ *   per query row and uses no workspace.
  * Requirements: d == 128 for BF16 (d in {64, 128} for F32), N >= 1, K >= 0;
  * with BF16, q, kv_cache and o 16-byte aligned (SATTN_ERR_INVALID_ARG
  * otherwise).
@@ -126,7 +133,9 @@ sattn_status sattn_sparse_fwd(const void *q, const void *kv_cache, const int32_t
                               int32_t K, void *workspace, size_t workspace_bytes,
                               sattn_dtype dtype, void *cuda_stream);
 
-/* Workspace size (bytes) that lets sattn_sparse_fwd split each index list. */
+/* Workspace size (bytes) that lets sattn_sparse_fwd's persistent kernel split
+ * each index list (an upper bound for any GPU of at most 256 SMs); calls that
+ * take the cluster path ignore the workspace. 0 when no split is possible. */
 size_t sattn_sparse_workspace_bytes(int32_t B, int32_t M, int32_t H, int32_t d, int32_t K);
 
 /* Size in bytes of the scratch array built into the library for
@@ -291,8 +300,9 @@ sattn_status sattn_quantize_kv_fp8(const void *kv, uint8_t *kv_nope, void *kv_ro
  * bf16 in shared memory (e4m3 value * scale, rounded to nearest even), so a
  * gathered row costs d - rd + 2 rd + 4 bytes instead of 2 d.
  * Supported: H = 32, d = 128, rd = 64 (SATTN_ERR_UNSUPPORTED otherwise);
- * q, kv_nope, kv_rope and o 16-byte aligned. Workspace as for sattn_sparse_fwd
- * (sattn_sparse_workspace_bytes).
+ * q, kv_nope, kv_rope and o 16-byte aligned. Execution and workspace as for
+ * sattn_sparse_fwd with bf16 (few queries: the cluster path, no workspace;
+ * otherwise the persistent kernel, split through the workspace if given).
  */
 sattn_status sattn_sparse_fp8_fwd(const void *q, const uint8_t *kv_nope, const void *kv_rope,
                                   const float *kv_scale, const int32_t *topk_idxs,
