@@ -232,6 +232,27 @@ __host__ __device__ constexpr uint32_t koff(int kk, uint32_t half) {
 // MN-major operand (V: rows = keys, 64-column halves of d KV_HALF bytes apart)
 __host__ __device__ constexpr uint32_t mnoff(int kk) { return (uint32_t)kk * 2048u >> 4; }
 
+// 3-D tiled TMA store from shared memory (bulk group), its commit and waits.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, uint32_t src, int x, int y,
+                                             int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(m)),
+        "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// this thread's bulk stores are complete
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 constexpr uint32_t IDESC_S = idesc_bf16_f32(128, BN, 0, 0);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, HD, 0, 1);
 
@@ -433,7 +454,8 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
 // ------------------------------------------------------------------ softmax / epilogue
 
 template <int MODE>
-__device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile int *abort,
+__device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slot, Bars &b,
+                             volatile int *abort,
                              uint32_t tmem, int first, int stride, const DevCtx &ctx) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;
@@ -459,9 +481,12 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
         const size_t roff = MODE == MODE_BLOCK ? pe.row_off : 0;
         const size_t orow = roff + (size_t)(pe.q_row0 + r) * p.H + pe.h;
         // Each pass covers 128 bytes of every row: this thread's row goes to
-        // the warp's staging buffer (128B-swizzled, conflict-free), then the
-        // warp writes 4 whole rows (4 lines) per store instruction.
+        // the warp's staging buffer (128B-swizzled, conflict-free). Window
+        // warps whose 32 rows all belong to the item hand the buffer to one
+        // bulk tensor store; otherwise the warp writes 4 whole rows (4 lines)
+        // per store instruction, skipping rows past the item.
         {
+            const bool bulk = MODE == MODE_WINDOW && quarter * 32 + 32 <= pe.nq;
             const uint32_t sb = smem_u32(slot.stage[quarter]);
             constexpr int PASSES = MODE == MODE_WINDOW ? 2 : 4;  // bf16: 64 d, fp32: 32 d per pass
             constexpr int ROW_BYTES = MODE == MODE_WINDOW ? HD * 2 : HD * 4;
@@ -493,12 +518,25 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&b.o_empty));
                 }
+                if (MODE == MODE_WINDOW) {  // an earlier bulk store may still read the buffer
+                    if (lane == 0) bulk_wait_read();
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
                                      sb + (uint32_t)lane * 128u + (((uint32_t)u ^ (lane & 7u)) << 4)),
                                  "r"(w[4 * u]), "r"(w[4 * u + 1]), "r"(w[4 * u + 2]), "r"(w[4 * u + 3])
                                  : "memory");
+                if (bulk) {
+                    fence_proxy_async_smem();  // the rows are read by the bulk copy
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(to, sb, pass * 64, pe.h, pe.q_row0 + quarter * 32);
+                        bulk_commit();
+                    }
+                    continue;
+                }
                 __syncwarp();
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -702,11 +740,13 @@ __device__ void softmax_role(const TcParams &p, Slot &slot, Bars &b, volatile in
                     MODE == MODE_BLOCK ? (size_t)it.L * p.M * p.H : 0};
     }
     if (ok && pend.valid) epilogue(pend);
+    if (MODE == MODE_WINDOW && lane == 0) bulk_wait_all();  // before the CTA's shared memory goes
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap to,
                const __grid_constant__ CUtensorMap tv, const TcParams p, const DevCtx ctx) {
     extern __shared__ __align__(1024) uint8_t dsmem[];
     Smem &sm = *reinterpret_cast<Smem *>(dsmem);
@@ -768,7 +808,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
         }
         __syncwarp();
     } else {
-        softmax_role<MODE>(p, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride, ctx);
+        softmax_role<MODE>(p, &to, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride,
+                           ctx);
     }
     tc_fence_before();
     __syncthreads();
@@ -794,10 +835,14 @@ template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int 
     TcParams p = p_in;
     for (const void *ptr : {q, k, v})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return cudaErrorMisalignedAddress;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (make_map(&tq, q, q_rows, p.H, BM) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (make_map(&tk, k, kv_rows, p.Hkv, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     if (make_map(&tv, v, kv_rows, p.Hkv, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // window: o [T, H, d] bf16 in 32-row boxes for the epilogue's bulk stores
+    // (block mode writes its fp32 partials with plain stores; the map is unused)
+    if (make_map(&to, MODE == MODE_WINDOW ? (const void *)p.o : q, q_rows, p.H, 32) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
     cudaError_t e = ensure_smem_attr((const void *)attn_tc_kernel<MODE>, smem, dev);
     if (e != cudaSuccess) return e;
@@ -809,7 +854,7 @@ template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int 
         fprintf(stderr, "sattn: attn_tc_kernel<%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",
                 MODE == MODE_WINDOW ? "window" : "block", grid, NTHREADS, smem, NSLOTS,
                 p.num_items);
-    attn_tc_kernel<MODE><<<grid, NTHREADS, smem, s>>>(tq, tk, tv, p, ctx);
+    attn_tc_kernel<MODE><<<grid, NTHREADS, smem, s>>>(tq, tk, to, tv, p, ctx);
     return cudaGetLastError();
 }
 
