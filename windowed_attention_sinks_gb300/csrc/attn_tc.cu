@@ -20,8 +20,8 @@
 //                 (A operand in tensor memory, two P buffers of 32 columns).
 //   warps 4+4s..  softmax + epilogue (four warps): thread = query row = TMEM lane. Each
 //                 row keeps its running max m and sum l in the log2 domain. An item's
-//                 epilogue runs after the first tile of the next item, so the
-//                 softmax is busy while the item's last P V drains.
+//                 epilogue runs once its last P V has completed, while the MMA
+//                 computes the next item's first scores.
 // S of tile j+1 is computed as soon as the softmax has loaded S of tile j.
 // No tensor-memory column is read by one MMA and written by a later one, so
 // ordering rests only on commits and barriers; since S of tile j is issued
@@ -464,16 +464,15 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
     const uint32_t o_tmem = tmem + O_COL + lane_off;
     int sc = 0, pc = 0, qi = 0;  // sc: tiles seen, pc: P tiles written
     bool ok = true;
-    // The epilogue of an item runs after the first tile of the next one: the
-    // softmax works on that tile while the item's last P V drains.
-    struct Pend {
-        bool valid;
+    // The epilogue of an item runs as soon as the item's last P V has
+    // completed; the MMA thread issues the next item's first S right after
+    // that P V, so those scores are computed while the epilogue runs.
+    struct Out {
         int q_row0, nq, h;
         float m, l;
         size_t row_off;  // block: the chunk's first output row
     };
-    Pend pend{false, 0, 0, 0, 0.f, 0.f};
-    auto epilogue = [&](const Pend &pe) -> bool {
+    auto epilogue = [&](const Out &pe) -> bool {
         if (!mbar_wait(smem_u32(&b.o_full), qi & 1, ctx, abort)) return false;
         tc_fence_after();
         const float inv = pe.l > 0.0f ? 1.0f / pe.l : 0.0f;
@@ -730,16 +729,11 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&b.p_full[pc & 1]));
             ++pc;
-            if (j == 0 && pend.valid) {
-                if (!(ok = epilogue(pend))) break;
-                pend.valid = false;
-            }
         }
         if (!ok) break;
-        pend = Pend{true, it.q_row0, it.nq, it.h, m_run, l,
-                    MODE == MODE_BLOCK ? (size_t)it.L * p.M * p.H : 0};
+        ok = epilogue(Out{it.q_row0, it.nq, it.h, m_run, l,
+                          MODE == MODE_BLOCK ? (size_t)it.L * p.M * p.H : 0});
     }
-    if (ok && pend.valid) epilogue(pend);
     if (MODE == MODE_WINDOW && lane == 0) bulk_wait_all();  // before the CTA's shared memory goes
 }
 
