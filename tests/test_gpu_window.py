@@ -94,6 +94,21 @@ def test_window_asymmetric_and_causal(wl, wr, causal):
         compare(o, lse, ro, rl, TOL_BF16_O, what="wl=%d wr=%d causal=%d" % (wl, wr, causal))
 
 
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (16, 2), (16, 1), (12, 2), (12, 4), (6, 2)])
+def test_query_head_packing(H, Hkv):
+    """The query heads of a KV group share a tile (two, four or eight of them:
+    the largest power of two dividing H / Hkv); groups of 3 run one head per
+    tile, groups of 6 two. Ragged sequences put every packed layout across
+    sequence ends and partial warp tiles."""
+    for wl, wr, causal in [(128, 128, 0), (37, 5, 1), (-1, -1, 1), (0, 300, 0)]:
+        case = _custom_case(EDGE_LENS, H, Hkv, 128, wl, wr, causal, "bf16", seed=H * 10 + Hkv)
+        for mode in (1, 2):
+            o, lse = run_window(case, mode)
+            ro, rl = oracle_window(case, mode)
+            compare(o, lse, ro, rl, TOL_BF16_O,
+                    what="H=%d Hkv=%d wl=%d wr=%d causal=%d mode=%d" % (H, Hkv, wl, wr, causal, mode))
+
+
 def test_large_logits_rescale():
     """Scores spread over a wide range force the running max to move by large
     steps inside a row (exercises the rescaling of the accumulator)."""
@@ -106,12 +121,14 @@ def test_large_logits_rescale():
         compare(o, lse, ro, rl, TOL_BF16_O, tol_lse=2e-3, what="large logits mode=%d" % mode)
 
 
-@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 64)])
-def test_mask_decisions_bit_exact(dtype, d):
+@pytest.mark.parametrize("dtype,d,H,Hkv", [("bf16", 128, 4, 2), ("f32", 64, 4, 2),
+                                           ("bf16", 128, 8, 1), ("bf16", 128, 8, 2)])
+def test_mask_decisions_bit_exact(dtype, d, H, Hkv):
     """q = 0 and one-hot values: the support of each output row is exactly the
-    set of visible keys, so the zero pattern must equal the oracle's bit for bit."""
+    set of visible keys, so the zero pattern must equal the oracle's bit for bit
+    (bf16 d = 128 runs the tensor-core kernel with 2, 8 and 4 query heads per tile)."""
     lens = [1, 5, 37, 128, 129, 200]
-    case = _custom_case(lens, 4, 2, d, 8, 8, 0, dtype)
+    case = _custom_case(lens, H, Hkv, d, 8, 8, 0, dtype)
     case.q[:] = 0
     case.v[:] = 0
     for s in range(len(lens)):

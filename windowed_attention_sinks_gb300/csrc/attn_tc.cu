@@ -9,7 +9,10 @@
 //    Stream Synchronization Fix": per-chunk partial stats, merged later);
 //    the key tiles are the two 64-key halves of each selected 128-key block.
 //
-// A work item is (128-query tile, query head). A persistent grid of one CTA
+// A work item is a tile of 128 query rows: in window mode BM / G tokens x G
+// query heads of one KV group (G, the largest power of two dividing H / Hkv
+// up to 8, shrinks the tile's key band and lets one K/V tile serve G heads),
+// in block mode 128 tokens of one head. A persistent grid of one CTA
 // per SM (kernels that allocate tensor memory run one CTA per SM) walks the
 // items with two independent pipeline slots, each with its own shared
 // memory, barriers, 256 TMEM columns and item stream. Per slot:
@@ -76,6 +79,10 @@ struct TcParams {
     // window
     const int32_t *cu_seqlens;
     int num_seqs, T, tiles_per_seq, wl, wr, causal;
+    // query heads per item: 1 << gshift heads that share a KV head fill the
+    // 128 tile rows together (row r = token r >> gshift, head r & (G - 1));
+    // hslots = H >> gshift items per token tile. Block mode: gshift = 0.
+    int gshift, hslots;
     const float *sinks;
     int sink_mode;
     __nv_bfloat16 *o;
@@ -99,7 +106,7 @@ struct Item {
                    // block: the chunk's keys [lo, hi) and the chunk's index
     const uint8_t *mrow;
     int kb_lo, kb_hi, kend;  // block: 128-key block range, key limit
-    float sink;              // window: the head's sink (0 when there is none)
+    float sink[8];           // window: the sinks of heads h .. h + G - 1 (0 without sinks)
 };
 
 struct Bars {
@@ -142,31 +149,35 @@ template <int MODE> __device__ __forceinline__ Item decode_item(const TcParams &
     it.valid = false;
     it.seq_err = false;
     it.ntiles = 0;
-    it.sink = 0.f;
-    it.h = v % p.H;
+    const int hslots = MODE == MODE_WINDOW ? p.hslots : p.H;
+    it.h = (v % hslots) << (MODE == MODE_WINDOW ? p.gshift : 0);  // first head of the item
     it.g = it.h / p.groups;
-    const int rest = v / p.H;
+    const int rest = v / hslots;
     if (MODE == MODE_WINDOW) {
+        const int TT = BM >> p.gshift;  // tokens per tile
         const int t = rest % p.tiles_per_seq, s = rest / p.tiles_per_seq;
         const int s0 = __ldg(p.cu_seqlens + s), s1 = __ldg(p.cu_seqlens + s + 1);
         if (s0 < 0 || s1 < s0 || s1 > p.T || __ldg(p.cu_seqlens) != 0 ||
-            s1 - s0 > p.tiles_per_seq * BM) {
+            s1 - s0 > p.tiles_per_seq * TT) {
             it.seq_err = true;
             return it;
         }
         it.L = s1 - s0;
-        const int qs = t * BM;
+        const int qs = t * TT;
         if (qs >= it.L) return it;
-        it.nq = min(BM, it.L - qs);
+        const int ntok = min(TT, it.L - qs);
+        it.nq = ntok << p.gshift;  // valid rows (token-major, so a prefix)
         it.q_row0 = s0 + qs;
         it.key_row0 = s0;
         it.qpos0 = qs;
-        const int last = qs + it.nq - 1;
+        const int last = qs + ntok - 1;
         it.lo = p.wl < 0 ? 0 : max(0, qs - p.wl);
         it.hi = p.wr < 0 ? it.L - 1 : min(it.L - 1, last + p.wr);
         if (p.causal) it.hi = min(it.hi, last);
         it.ntiles = (it.hi - it.lo + BN) / BN;
-        it.sink = p.sinks ? __ldg(p.sinks + it.h) : 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)  // constant indices keep the item in registers
+            it.sink[i] = p.sinks && i < (1 << p.gshift) ? __ldg(p.sinks + it.h + i) : 0.f;
         it.valid = true;
     } else {
         const int qb = rest % p.QB;
@@ -330,7 +341,7 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
             } else if (MODE == MODE_WINDOW && v >= v_static) {
                 // every later item of this sequence lies past its end as well:
                 // move the counter to the next sequence's first item
-                const int per_seq = p.H * p.tiles_per_seq;
+                const int per_seq = p.hslots * p.tiles_per_seq;
                 atomicMax(p.work, (unsigned)((v / per_seq + 1) * per_seq - v_static));
             }
             continue;
@@ -460,6 +471,9 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // query row within the tile == TMEM lane
+    // the row's token (from the tile's first) and head (from the item's first)
+    const int gs = MODE == MODE_WINDOW ? p.gshift : 0;
+    const int tok = r >> gs, hl = r & ((1 << gs) - 1);
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t o_tmem = tmem + O_COL + lane_off;
     int sc = 0, pc = 0, qi = 0;  // sc: tiles seen, pc: P tiles written
@@ -478,7 +492,7 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
         const float inv = pe.l > 0.0f ? 1.0f / pe.l : 0.0f;
         // block: the chunk's rows; window: no offset (folded at compile time)
         const size_t roff = MODE == MODE_BLOCK ? pe.row_off : 0;
-        const size_t orow = roff + (size_t)(pe.q_row0 + r) * p.H + pe.h;
+        const size_t orow = roff + (size_t)(pe.q_row0 + tok) * p.H + pe.h + hl;
         // Each pass covers 128 bytes of every row: this thread's row goes to
         // the warp's staging buffer (128B-swizzled, conflict-free). Window
         // warps whose 32 rows all belong to the item hand the buffer to one
@@ -531,7 +545,7 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
                     fence_proxy_async_smem();  // the rows are read by the bulk copy
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(to, sb, pass * 64, pe.h, pe.q_row0 + quarter * 32);
+                        tma_store_3d(to, sb, pass * 64, pe.h, pe.q_row0 + ((quarter * 32) >> gs));
                         bulk_commit();
                     }
                     continue;
@@ -546,7 +560,8 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
                                  : "r"(sb + (uint32_t)rw * 128u + (((uint32_t)unit ^ ((uint32_t)rw & 7u)) << 4)));
                     const int rr = quarter * 32 + rw;
                     if (rr < pe.nq) {
-                        const size_t grow = roff + (size_t)(pe.q_row0 + rr) * p.H + pe.h;
+                        const size_t grow = roff + (size_t)(pe.q_row0 + (rr >> gs)) * p.H + pe.h +
+                                            (rr & ((1 << gs) - 1));
                         *reinterpret_cast<uint4 *>(obase + grow * ROW_BYTES + pass * 128 + unit * 16) = v;
                     }
                 }
@@ -571,13 +586,14 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
             break;
         }
         const Item it = b.item[slot_k];
+        const float sink = MODE == MODE_WINDOW ? b.item[slot_k].sink[hl] : 0.f;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&b.item_empty[slot_k]));
         if (!it.valid) break;
         const bool row_valid = r < it.nq;
         if (it.ntiles == 0) {  // block mode: nothing visible in this chunk
             if (MODE == MODE_BLOCK && row_valid) {
-                const size_t orow = (size_t)it.L * p.M * p.H + (size_t)(it.q_row0 + r) * p.H + it.h;
+                const size_t orow = (size_t)it.L * p.M * p.H + (size_t)(it.q_row0 + tok) * p.H + it.h + hl;
                 float4 *dst = reinterpret_cast<float4 *>(p.o_part + orow * HD);
 #pragma unroll 8
                 for (int i = 0; i < HD / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -587,7 +603,7 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
         }
         const bool warp_all_valid = __all_sync(FULL, row_valid);
         // visible key interval of this row (window: fixed for the item)
-        const int qi_loc = it.qpos0 + r;
+        const int qi_loc = it.qpos0 + tok;
         constexpr int NONE_LO = 1 << 30, NONE_HI = -(1 << 30);  // empty interval
         int lo_r = NONE_LO, hi_r = NONE_HI;
         if (MODE == MODE_WINDOW && row_valid) {
@@ -597,7 +613,6 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
         }
         const bool null_sink = MODE == MODE_WINDOW && p.sink_mode == 2;
         const bool key0 = MODE == MODE_WINDOW && p.sink_mode == 1;
-        const float sink = MODE == MODE_WINDOW ? it.sink : 0.f;
         float m_run = null_sink ? sink * LOG2E : -INFINITY;
         float l = null_sink ? 1.0f : 0.0f;
         const uint64_t scale2 = f2_pack(p.scale_l2, p.scale_l2);
@@ -815,10 +830,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
 
 // ------------------------------------------------------------------ host side
 
-CUresult make_map(CUtensorMap *m, const void *base, int rows, int heads, uint32_t box_rows) {
+CUresult make_map(CUtensorMap *m, const void *base, int rows, int heads, uint32_t box_heads,
+                  uint32_t box_rows) {
     const uint64_t dims[3] = {(uint64_t)HD, (uint64_t)heads, (uint64_t)rows};
     const uint64_t strides[2] = {(uint64_t)HD * 2, (uint64_t)HD * 2 * heads};
-    const uint32_t box[3] = {64, 1, box_rows};
+    const uint32_t box[3] = {64, box_heads, box_rows};
     return encode_tensor_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                              strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -830,12 +846,15 @@ template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int 
     for (const void *ptr : {q, k, v})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return cudaErrorMisalignedAddress;
     CUtensorMap tq, tk, tv, to;
-    if (make_map(&tq, q, q_rows, p.H, BM) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (make_map(&tk, k, kv_rows, p.Hkv, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    if (make_map(&tv, v, kv_rows, p.Hkv, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // Q tiles: 128 rows = BM >> gshift tokens x (1 << gshift) heads, token-major
+    const int G = 1 << p.gshift;
+    if (make_map(&tq, q, q_rows, p.H, G, BM / G) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (make_map(&tk, k, kv_rows, p.Hkv, 1, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (make_map(&tv, v, kv_rows, p.Hkv, 1, BN) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     // window: o [T, H, d] bf16 in 32-row boxes for the epilogue's bulk stores
     // (block mode writes its fp32 partials with plain stores; the map is unused)
-    if (make_map(&to, MODE == MODE_WINDOW ? (const void *)p.o : q, q_rows, p.H, 32) != CUDA_SUCCESS)
+    if (make_map(&to, MODE == MODE_WINDOW ? (const void *)p.o : q, q_rows, p.H, G, 32 / G) !=
+        CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
     cudaError_t e = ensure_smem_attr((const void *)attn_tc_kernel<MODE>, smem, dev);
@@ -864,7 +883,14 @@ cudaError_t launch_window_tc(const WindowArgs &a, const DevInfo &dev, cudaStream
     p.cu_seqlens = a.cu_seqlens;
     p.num_seqs = a.num_seqs;
     p.T = a.T;
-    p.tiles_per_seq = (a.max_seqlen + BM - 1) / BM;
+    // Query heads that share a KV head are packed into one tile (the largest
+    // power of two dividing H / Hkv, at most 8): a tile of BM / G tokens has a
+    // narrower key band than one of BM tokens, and its K/V tiles serve G heads.
+    int gs = 0;
+    while (gs < 3 && p.groups % (2 << gs) == 0) ++gs;
+    p.gshift = gs;
+    p.hslots = a.H >> gs;
+    p.tiles_per_seq = (a.max_seqlen + (BM >> gs) - 1) / (BM >> gs);
     p.wl = a.wl;
     p.wr = a.wr;
     p.causal = a.causal;
@@ -872,7 +898,7 @@ cudaError_t launch_window_tc(const WindowArgs &a, const DevInfo &dev, cudaStream
     p.sink_mode = a.sink_mode;
     p.o = static_cast<__nv_bfloat16 *>(a.o);
     p.lse = a.lse;
-    const long long items = (long long)a.num_seqs * p.tiles_per_seq * a.H;
+    const long long items = (long long)a.num_seqs * p.tiles_per_seq * p.hslots;
     if (items > INT_MAX) return cudaErrorInvalidValue;
     p.num_items = (int)items;
     if (reinterpret_cast<uintptr_t>(a.o) & 15u) return cudaErrorMisalignedAddress;
