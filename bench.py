@@ -488,9 +488,17 @@ def build_path(workload, seed, device, stream):
         cache = torch.zeros((1, win + 8192, d), dtype=bf, device=device)
         new_kv = torch.randn((1, M, d), device=device).to(bf)
 
+        side = torch.cuda.Stream(device=device)
+
         def launch(st=None):
-            sa.build_topk_idxs(starts, M, K, win, ratio, out=idx_out, stream=st or stream)
-            sa.kv_ring_write(cache, new_kv, starts, win, stream=st or stream)
+            # the two are independent (the lists do not read the ring): the ring
+            # write runs on a second stream, joined before the step ends
+            s0 = st or stream
+            side.wait_stream(s0)
+            sa.build_topk_idxs(starts, M, K, win, ratio, out=idx_out, stream=s0)
+            with torch.cuda.stream(side):
+                sa.kv_ring_write(cache, new_kv, starts, win, stream=side)
+            s0.wait_stream(side)
         # the 67 MB of lists fit in L2: a larger scratch is rewritten before each step
         return Path(launch=launch, units=M, nbytes=idx_out.numel() * 4 + 2 * win * d * 2,
                     flops=0, flush=True, graph=True, launches=2, kernel="topk_idxs_kernel",
