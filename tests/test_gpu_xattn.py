@@ -209,6 +209,35 @@ def test_find_blocks_counts_negative_and_nan_sums_as_zero():
         assert not want[0, 0].any()
 
 
+@pytest.mark.parametrize("kind,KB", [("narrow", 200), ("narrow", 256), ("wide", 200),
+                                     ("subnormal", 256), ("ties", 256), ("narrow", 300)])
+def test_find_blocks_exact_on_both_paths(kind, KB):
+    """Rows of at most 256 blocks whose masses lie within 2^21 of each other
+    take the kernel's parallel integer prefix sums; wider spans and longer
+    rows the sequential float64 walk. Both must match the oracle decision for
+    decision, ties and exact boundaries included (the threshold is passed to
+    the oracle rounded to float32, as the kernel receives it)."""
+    rng = np.random.default_rng(KB + len(kind))
+    H, QB = 3, 7
+    if kind == "narrow":
+        bs = (rng.random((H, QB, KB)) + 0.01).astype(np.float32)
+    elif kind == "wide":
+        bs = (10.0 ** rng.uniform(-30, 0, (H, QB, KB))).astype(np.float32)
+    elif kind == "subnormal":  # masses below the smallest normal float, and a few just above
+        bs = (rng.random((H, QB, KB)) * 1e-39).astype(np.float32)
+        bs[:, :, ::17] = np.float32(2e-38)
+    else:  # equal masses and running sums that hit the target exactly
+        bs = rng.choice(np.float32([0.0, 0.125, 0.25, 0.5]), (H, QB, KB))
+    bs[0, 0, :] = 0.0  # a row with no mass
+    for thr in (0.0, 0.25, 0.3, 0.5, 0.75, 0.9, 0.999, 1.0):
+        t32 = float(np.float32(thr))
+        mask = sa.xattn_find_blocks(torch.from_numpy(bs).cuda(), t32)
+        sa.check_device()
+        want = oracle.xattn_find_blocks(bs, t32)
+        assert np.array_equal(mask.cpu().numpy(), want), (kind, KB, thr)
+        assert not want[0, 0].any()
+
+
 def test_selection_flips_against_fp64_block_sums():
     # the kernel's fp32 block sums against the oracle's fp64 ones: thresholding
     # is discontinuous, so a block whose cumulative mass sits at the threshold

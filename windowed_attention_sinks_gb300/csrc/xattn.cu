@@ -484,9 +484,19 @@ __global__ void merge_stats_kernel(const float *__restrict__ m_parts,
 // Step 4: one CTA per (head, query block). The key blocks are sorted by
 // (mass descending, block ascending) with a bitonic sort of 64-bit keys in
 // shared memory (masses are taken as >= 0, so their bit patterns order like
-// the values); one thread then walks them in that order with float64 sums.
+// the values); the selection then takes the shortest leading run whose
+// float64 running sum, taken in that order, reaches threshold x the total.
+//
+// Fast path (at most FB_THREADS blocks, nonzero masses within 2^21 of each
+// other): every mass is an integer multiple of 2^(emin - 150), emin the
+// smallest biased exponent among them, below 2^(24 + 21); a running sum of
+// at most 256 of them stays below 2^53 units, so each float64 running sum is
+// exact and equals the integer prefix sum, which the CTA computes with a
+// parallel scan. Otherwise one thread walks the blocks with float64 sums.
+// Both give the same decisions.
 constexpr int FB_THREADS = 256;
 constexpr int FB_MAX = 4096;  // key blocks per row supported
+constexpr int FB_SPAN = 53 - 24 - 8;  // exponent span of the fast path (256 terms)
 
 __global__ void __launch_bounds__(FB_THREADS)
 find_blocks_kernel(const float *__restrict__ block_sum, int KB, float threshold,
@@ -524,6 +534,54 @@ find_blocks_kernel(const float *__restrict__ block_sum, int KB, float threshold,
             __syncthreads();
         }
     }
+    // ---- fast path: integer prefix sums (thread t holds sorted position t)
+    __shared__ int s_emin, s_emax, s_first;
+    __shared__ long long s_warp[FB_THREADS / 32];
+    if (threadIdx.x == 0) {
+        s_emin = 1 << 30;
+        s_emax = -1;
+        s_first = KB;
+    }
+    __syncthreads();
+    const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
+    const uint32_t u = t < KB ? 0xffffffffu - (uint32_t)(keys[t] >> 32) : 0u;  // mass bits
+    const int be = (int)(u >> 23);                                            // biased exponent
+    if (KB <= FB_THREADS && u != 0u) {
+        atomicMin(&s_emin, be > 0 ? be : 1);
+        atomicMax(&s_emax, be);
+    }
+    __syncthreads();
+    const int emin = s_emin, emax = s_emax;
+    if (KB <= FB_THREADS && emax < 0) return;  // no mass: nothing selected
+    if (KB <= FB_THREADS && emax < 255 && emax - emin <= FB_SPAN) {
+        // the mass in units of 2^(emin - 150): significand shifted by its exponent's excess
+        const long long mant = (long long)((u & 0x7fffffu) | (be > 0 ? 0x800000u : 0u));
+        long long x = u != 0u ? mant << ((be > 0 ? be : 1) - emin) : 0ll;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {  // inclusive scan within the warp
+            const long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp[wid] = x;
+        __syncthreads();
+        long long before = 0;
+        for (int w = 0; w < wid; ++w) before += s_warp[w];
+        long long total = 0;
+        for (int w = 0; w < FB_THREADS / 32; ++w) total += s_warp[w];
+        const long long prefix = before + x;  // running sum through sorted position t
+        if (total > 0) {
+            const double unit = ldexp(1.0, emin - 150);
+            const double target = (double)threshold * ((double)total * unit);
+            if (t < KB && (double)prefix * unit >= target) atomicMin(&s_first, t);
+            __syncthreads();
+            // all blocks up to the first position that reaches the target
+            // (all of them if none does)
+            const int last = s_first < KB ? s_first : KB - 1;
+            if (t <= last) out[(unsigned)(keys[t] & 0xffffffffu)] = 1;
+        }
+        return;
+    }
+    // ---- otherwise: one thread, float64 running sums in sorted order
     if (threadIdx.x == 0) {
         double total = 0.0;
         for (int i = 0; i < KB; ++i) total += (double)__uint_as_float(0xffffffffu - (unsigned)(keys[i] >> 32));
