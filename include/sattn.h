@@ -91,8 +91,11 @@ typedef enum { SATTN_F32 = 0, SATTN_BF16 = 1 } sattn_dtype;
  * unbounded on that side) and, if causal, j <= i. Query head h reads KV head
  * h / (H / Hkv). Logits are scale * <q, k> with scale > 0. o has q's dtype (round to
  * nearest even for bf16). With dtype BF16 and d = 128 the tcgen05 kernel
- * runs; other combinations run the SIMT kernel.
- * Requirements: H % Hkv == 0, d in {64, 128}, num_seqs >= 0.
+ * runs (the query heads of a KV group share its 128-row tiles: the largest
+ * power of two dividing H / Hkv, at most 8, of them); other combinations run
+ * the SIMT kernel.
+ * Requirements: H % Hkv == 0, d in {64, 128}, num_seqs >= 0; with BF16 and
+ * d = 128, q, k, v and o 16-byte aligned (SATTN_ERR_INVALID_ARG otherwise).
  */
 sattn_status sattn_window_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                               const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
