@@ -144,6 +144,26 @@ def test_mask_decisions_bit_exact(dtype, d, H, Hkv):
             compare(o, lse, ro, rl, TOL_BF16_O if dtype == "bf16" else TOL_F32_O)
 
 
+def test_misaligned_tensors_are_refused():
+    """The tensor-core path reads q, k, v and writes o through TMA, which needs
+    16-byte aligned bases: a misaligned one is an invalid argument, reported
+    before any launch."""
+    case = _custom_case([40, 7], 4, 2, 128, 8, 8, 0, "bf16")
+    q, k, v = dev(case.q, torch.bfloat16), dev(case.k, torch.bfloat16), dev(case.v, torch.bfloat16)
+    cu = dev(case.cu_seqlens, torch.int32)
+    buf = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    o_bad = buf[1:1 + q.numel()].view(q.shape)  # 2 bytes past a 16-byte boundary
+    q_bad = buf[1:1 + q.numel()].view(q.shape).copy_(q)
+    for kw, args in (({"o": o_bad}, (q, k, v)), ({}, (q_bad, k, v))):
+        with pytest.raises(sa.SattnError) as e:
+            sa.window_fwd(*args, cu, case.max_seqlen, 8, 8, False, None, 0, case.scale, **kw)
+        assert e.value.code == 1
+    o, lse = sa.window_fwd(q, k, v, cu, case.max_seqlen, 8, 8, False, None, 0, case.scale)
+    sa.check_device()
+    ro, rl = oracle_window(case, 0)
+    compare(o, lse, ro, rl, TOL_BF16_O, what="after refused calls")
+
+
 def test_sink_reductions_on_gpu():
     """key-0 sink 0 and null sink -inf reproduce the no-sink output on the GPU."""
     case = W.window_vision_bf16(2, 8, num_seqs=3)
