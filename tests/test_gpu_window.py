@@ -109,6 +109,19 @@ def test_query_head_packing(H, Hkv):
                     what="H=%d Hkv=%d wl=%d wr=%d causal=%d mode=%d" % (H, Hkv, wl, wr, causal, mode))
 
 
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (8, 2), (8, 1)])
+def test_long_sequence_full_causal(H, Hkv):
+    """One long sequence with unbounded causal attention: items of about 70 key
+    tiles, the running max moving many times per row, and a second short
+    sequence after it in the same batch."""
+    case = _custom_case([4500, 77], H, Hkv, 128, -1, -1, 1, "bf16", seed=H + 7 * Hkv, std=1.5)
+    for mode in (1, 2):
+        o, lse = run_window(case, mode)
+        ro, rl = oracle_window(case, mode)
+        compare(o, lse, ro, rl, TOL_BF16_O, tol_lse=2e-3,
+                what="long causal H=%d Hkv=%d mode=%d" % (H, Hkv, mode))
+
+
 def test_large_logits_rescale():
     """Scores spread over a wide range force the running max to move by large
     steps inside a row (exercises the rescaling of the accumulator)."""
