@@ -94,7 +94,8 @@ def test_window_asymmetric_and_causal(wl, wr, causal):
         compare(o, lse, ro, rl, TOL_BF16_O, what="wl=%d wr=%d causal=%d" % (wl, wr, causal))
 
 
-@pytest.mark.parametrize("H,Hkv", [(8, 2), (16, 2), (16, 1), (12, 2), (12, 4), (6, 2)])
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (16, 2), (16, 1), (12, 2), (12, 4), (6, 2), (1, 1),
+                                   (32, 4)])
 def test_query_head_packing(H, Hkv):
     """The query heads of a KV group share a tile (two, four or eight of them:
     the largest power of two dividing H / Hkv); groups of 3 run one head per
