@@ -385,7 +385,7 @@ __device__ void producer(const TcParams &p, const CUtensorMap *tq, const CUtenso
 
 // ------------------------------------------------------------------ MMA issuer
 
-template <int MODE>
+template <int MODE, bool LOOK>
 __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *abort,
                            uint32_t tmem, int first, int stride, const DevCtx &ctx) {
     int qi = 0, kt = 0, pc = 0;
@@ -399,62 +399,134 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
     const uint64_t dv0 = smem_desc_sw128(smem_u32(sm.v[0]), KV_HALF, 1024u);
     const uint64_t dv1 = smem_desc_sw128(smem_u32(sm.v[1]), KV_HALF, 1024u);
     if (ctx.stall) mbar_wait(smem_u32(&b.drain), 0, ctx, abort);  // test hook: runs out
-    for (int ic = 0; ok; ++ic) {
-        const int slot_k = ic % ITEM_RING;
-        if (!mbar_wait(smem_u32(&b.item_full[slot_k]), (ic / ITEM_RING) & 1, ctx, abort)) break;
-        const Item it = b.item[slot_k];
-        mbar_arrive(smem_u32(&b.item_empty[slot_k]));
-        if (!it.valid) break;
-        if (it.ntiles == 0) continue;
-        ok = mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort);
-        const int n = it.ntiles, kt0 = kt;
-        auto issue_pv = [&](int jj) -> bool {
+    if constexpr (!LOOK) {
+        for (int ic = 0; ok; ++ic) {
+            const int slot_k = ic % ITEM_RING;
+            if (!mbar_wait(smem_u32(&b.item_full[slot_k]), (ic / ITEM_RING) & 1, ctx, abort)) break;
+            const Item it = b.item[slot_k];
+            mbar_arrive(smem_u32(&b.item_empty[slot_k]));
+            if (!it.valid) break;
+            if (it.ntiles == 0) continue;
+            ok = mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort);
+            const int n = it.ntiles, kt0 = kt;
+            auto issue_pv = [&](int jj) -> bool {
+                const int st = (kt0 + jj) % VSTAGES, use = (kt0 + jj) / VSTAGES;
+                // the stage and O waits first, P (written by the softmax, the one
+                // this thread usually waits for) last: each barrier access of this
+                // thread stalls the MMAs in flight, so the last one should be the
+                // one that releases the issue
+                if (!mbar_wait(smem_u32(&b.v_full[st]), use & 1, ctx, abort)) return false;
+                if (jj == 0 && qi >= 1 &&
+                    !mbar_wait(smem_u32(&b.o_empty), (qi - 1) & 1, ctx, abort))
+                    return false;
+                if (!mbar_wait(smem_u32(&b.p_full[pc & 1]), (pc >> 1) & 1, ctx, abort)) return false;
+                tc_fence_after();
+                const uint64_t dv = st ? dv1 : dv0;
+                const uint32_t p_tmem = tmem + P_COL + 32u * (uint32_t)(pc & 1);
+                const uint32_t acc0 = jj > 0 ? 1u : 0u;
+    #pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    tc_mma_f16_ts(o_tmem, p_tmem + 8u * kk, dv + mnoff(kk), IDESC_PV,
+                                  kk > 0 ? 1u : acc0);
+                tc_commit(smem_u32(&b.v_empty[st]));
+                tc_commit(smem_u32(&b.pv_done));
+                ++pc;
+                return true;
+            };
+            for (int j = 0; ok && j < n; ++j) {
+                // one S buffer: tile t may start once the softmax has loaded tile t-1
+                const int t = kt0 + j, st = t % KSTAGES, use = t / KSTAGES;
+                // the key stage first, the softmax's release of S last (as above)
+                ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort);
+                if (ok && t >= 1) ok = mbar_wait(smem_u32(&b.s_empty), (t - 1) & 1, ctx, abort);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t dk = st ? dk1 : dk0;
+                const uint32_t s_tmem = tmem + S_COL;
+    #pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    tc_mma_f16(s_tmem, dq + koff(kk, Q_HALF), dk + koff(kk, KV_HALF), IDESC_S,
+                               kk > 0 ? 1u : 0u);
+                tc_commit(smem_u32(&b.k_empty[st]));
+                tc_commit(smem_u32(&b.s_full));
+                if (j == n - 1) tc_commit(smem_u32(&b.q_empty));
+                if (j >= 1) ok = issue_pv(j - 1);
+            }
+            if (ok) ok = issue_pv(n - 1);
+            if (ok) tc_commit(smem_u32(&b.o_full));
+            ++qi;
+            kt += n;
+        }
+    } else {
+        // Lookahead: an item's last P V is issued after the next item's first S,
+        // so that the next scores are computed while the softmax ends the item
+        // (which hides the next item's Q load). The softmax then defers that
+        // item's epilogue past the next item's first tile: the last P V waits for
+        // this thread to have taken the next item with key tiles from the ring,
+        // which the softmax must keep draining instead of waiting for O.
+        auto issue_pv = [&](int kt0, int jj, int q) -> bool {
             const int st = (kt0 + jj) % VSTAGES, use = (kt0 + jj) / VSTAGES;
-            // the stage and O waits first, P (written by the softmax, the one
-            // this thread usually waits for) last: each barrier access of this
-            // thread stalls the MMAs in flight, so the last one should be the
-            // one that releases the issue
             if (!mbar_wait(smem_u32(&b.v_full[st]), use & 1, ctx, abort)) return false;
-            if (jj == 0 && qi >= 1 &&
-                !mbar_wait(smem_u32(&b.o_empty), (qi - 1) & 1, ctx, abort))
+            if (jj == 0 && q >= 1 && !mbar_wait(smem_u32(&b.o_empty), (q - 1) & 1, ctx, abort))
                 return false;
             if (!mbar_wait(smem_u32(&b.p_full[pc & 1]), (pc >> 1) & 1, ctx, abort)) return false;
             tc_fence_after();
             const uint64_t dv = st ? dv1 : dv0;
             const uint32_t p_tmem = tmem + P_COL + 32u * (uint32_t)(pc & 1);
             const uint32_t acc0 = jj > 0 ? 1u : 0u;
-#pragma unroll
+    #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-                tc_mma_f16_ts(o_tmem, p_tmem + 8u * kk, dv + mnoff(kk), IDESC_PV,
-                              kk > 0 ? 1u : acc0);
+                tc_mma_f16_ts(o_tmem, p_tmem + 8u * kk, dv + mnoff(kk), IDESC_PV, kk > 0 ? 1u : acc0);
             tc_commit(smem_u32(&b.v_empty[st]));
             tc_commit(smem_u32(&b.pv_done));
             ++pc;
             return true;
         };
-        for (int j = 0; ok && j < n; ++j) {
-            // one S buffer: tile t may start once the softmax has loaded tile t-1
-            const int t = kt0 + j, st = t % KSTAGES, use = t / KSTAGES;
-            // the key stage first, the softmax's release of S last (as above)
-            ok = mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort);
-            if (ok && t >= 1) ok = mbar_wait(smem_u32(&b.s_empty), (t - 1) & 1, ctx, abort);
-            if (!ok) break;
+        auto issue_s = [&](int t, bool last_of_item) -> bool {
+            const int st = t % KSTAGES, use = t / KSTAGES;
+            if (!mbar_wait(smem_u32(&b.k_full[st]), use & 1, ctx, abort)) return false;
+            if (t >= 1 && !mbar_wait(smem_u32(&b.s_empty), (t - 1) & 1, ctx, abort)) return false;
             tc_fence_after();
             const uint64_t dk = st ? dk1 : dk0;
             const uint32_t s_tmem = tmem + S_COL;
-#pragma unroll
+    #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk)
                 tc_mma_f16(s_tmem, dq + koff(kk, Q_HALF), dk + koff(kk, KV_HALF), IDESC_S,
                            kk > 0 ? 1u : 0u);
             tc_commit(smem_u32(&b.k_empty[st]));
             tc_commit(smem_u32(&b.s_full));
-            if (j == n - 1) tc_commit(smem_u32(&b.q_empty));
-            if (j >= 1) ok = issue_pv(j - 1);
+            if (last_of_item) tc_commit(smem_u32(&b.q_empty));
+            return true;
+        };
+        int pend_kt0 = -1, pend_j = 0, pend_q = 0;  // pending last P V (pend_kt0 < 0: none)
+        auto flush = [&]() -> bool {
+            if (pend_kt0 < 0) return true;
+            if (!issue_pv(pend_kt0, pend_j, pend_q)) return false;
+            tc_commit(smem_u32(&b.o_full));
+            pend_kt0 = -1;
+            return true;
+        };
+        for (int ic = 0; ok; ++ic) {
+            const int slot_k = ic % ITEM_RING;
+            if (!mbar_wait(smem_u32(&b.item_full[slot_k]), (ic / ITEM_RING) & 1, ctx, abort)) {
+                ok = false;
+                break;
+            }
+            const Item it = b.item[slot_k];
+            mbar_arrive(smem_u32(&b.item_empty[slot_k]));
+            if (!it.valid) break;
+            if (it.ntiles == 0) continue;
+            const int n = it.ntiles, kt0 = kt;
+            ok = mbar_wait(smem_u32(&b.q_full), qi & 1, ctx, abort) && issue_s(kt0, n == 1) && flush();
+            for (int j = 1; ok && j < n; ++j)
+                ok = issue_s(kt0 + j, j == n - 1) && issue_pv(kt0, j - 1, qi);
+            pend_kt0 = kt0;
+            pend_j = n - 1;
+            pend_q = qi;
+            ++qi;
+            kt += n;
         }
-        if (ok) ok = issue_pv(n - 1);
-        if (ok) tc_commit(smem_u32(&b.o_full));
-        ++qi;
-        kt += n;
+        if (ok) ok = flush();
     }
     // Every tcgen05 operation issued above completes before TMEM is released.
     tc_commit(smem_u32(&b.drain));
@@ -464,7 +536,7 @@ __device__ void mma_issuer(const TcParams &p, Slot &sm, Bars &b, volatile int *a
 
 // ------------------------------------------------------------------ softmax / epilogue
 
-template <int MODE>
+template <int MODE, bool LOOK>
 __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slot, Bars &b,
                              volatile int *abort,
                              uint32_t tmem, int first, int stride, const DevCtx &ctx) {
@@ -486,6 +558,8 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
         float m, l;
         size_t row_off;  // block: the chunk's first output row
     };
+    Out pend{0, 0, 0, 0.f, 0.f, 0};
+    bool pend_valid = false;  // lookahead: the epilogue waits for the next item's first tile
     auto epilogue = [&](const Out &pe) -> bool {
         if (!mbar_wait(smem_u32(&b.o_full), qi & 1, ctx, abort)) return false;
         tc_fence_after();
@@ -744,15 +818,26 @@ __device__ void softmax_role(const TcParams &p, const CUtensorMap *to, Slot &slo
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&b.p_full[pc & 1]));
             ++pc;
+            if (LOOK && j == 0 && pend_valid) {
+                if (!(ok = epilogue(pend))) break;
+                pend_valid = false;
+            }
         }
         if (!ok) break;
-        ok = epilogue(Out{it.q_row0, it.nq, it.h, m_run, l,
-                          MODE == MODE_BLOCK ? (size_t)it.L * p.M * p.H : 0});
+        const Out out{it.q_row0, it.nq, it.h, m_run, l,
+                      MODE == MODE_BLOCK ? (size_t)it.L * p.M * p.H : 0};
+        if (LOOK) {
+            pend = out;
+            pend_valid = true;
+        } else {
+            ok = epilogue(out);
+        }
     }
+    if (LOOK && ok && pend_valid) epilogue(pend);
     if (MODE == MODE_WINDOW && lane == 0) bulk_wait_all();  // before the CTA's shared memory goes
 }
 
-template <int MODE>
+template <int MODE, bool LOOK>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap to,
@@ -812,12 +897,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ C
                 producer<MODE>(p, &tq, &tk, &tv, sm.slot[slot], sm.bars[slot], &sm.abort, first,
                                stride, ctx);
             else
-                mma_issuer<MODE>(p, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride,
+                mma_issuer<MODE, LOOK>(p, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride,
                                  ctx);
         }
         __syncwarp();
     } else {
-        softmax_role<MODE>(p, &to, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride,
+        softmax_role<MODE, LOOK>(p, &to, sm.slot[slot], sm.bars[slot], &sm.abort, tmem, first, stride,
                            ctx);
     }
     tc_fence_before();
@@ -839,7 +924,7 @@ CUresult make_map(CUtensorMap *m, const void *base, int rows, int heads, uint32_
                              strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int q_rows,
+template <int MODE, bool LOOK> cudaError_t launch(const TcParams &p_in, const void *q, int q_rows,
                                        const void *k, const void *v, int kv_rows,
                                        const DevInfo &dev, cudaStream_t s) {
     TcParams p = p_in;
@@ -857,17 +942,18 @@ template <int MODE> cudaError_t launch(const TcParams &p_in, const void *q, int 
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const size_t smem = sizeof(Smem);
-    cudaError_t e = ensure_smem_attr((const void *)attn_tc_kernel<MODE>, smem, dev);
+    cudaError_t e = ensure_smem_attr((const void *)attn_tc_kernel<MODE, LOOK>, smem, dev);
     if (e != cudaSuccess) return e;
     const int streams = (p.num_items + NSLOTS - 1) / NSLOTS;
     const int grid = streams < dev.sm_count ? streams : dev.sm_count;
     if (!(p.work = launch_claim_counter(dev, s, &e))) return e;
     const DevCtx ctx = make_ctx(dev);
     if (verbose())
-        fprintf(stderr, "sattn: attn_tc_kernel<%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",
-                MODE == MODE_WINDOW ? "window" : "block", grid, NTHREADS, smem, NSLOTS,
-                p.num_items);
-    attn_tc_kernel<MODE><<<grid, NTHREADS, smem, s>>>(tq, tk, to, tv, p, ctx);
+        fprintf(stderr,
+                "sattn: attn_tc_kernel<%s%s> grid=%d block=%d smem=%zu slots=%d items=%d\n",
+                MODE == MODE_WINDOW ? "window" : "block", LOOK ? ", lookahead" : "", grid,
+                NTHREADS, smem, NSLOTS, p.num_items);
+    attn_tc_kernel<MODE, LOOK><<<grid, NTHREADS, smem, s>>>(tq, tk, to, tv, p, ctx);
     return cudaGetLastError();
 }
 
@@ -902,7 +988,11 @@ cudaError_t launch_window_tc(const WindowArgs &a, const DevInfo &dev, cudaStream
     if (items > INT_MAX) return cudaErrorInvalidValue;
     p.num_items = (int)items;
     if (reinterpret_cast<uintptr_t>(a.o) & 15u) return cudaErrorMisalignedAddress;
-    return launch<MODE_WINDOW>(p, a.q, a.T, a.k, a.v, a.T, dev, s);
+    // packed heads make short items (fewer key tiles per row): there, issuing
+    // the next item's first S before an item's last P V measured faster; with
+    // one head per tile the plain order did
+    return p.gshift > 0 ? launch<MODE_WINDOW, true>(p, a.q, a.T, a.k, a.v, a.T, dev, s)
+                        : launch<MODE_WINDOW, false>(p, a.q, a.T, a.k, a.v, a.T, dev, s);
 }
 
 cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t s) {
@@ -932,7 +1022,7 @@ cudaError_t launch_block_tc(const BlockArgs &a, const DevInfo &dev, cudaStream_t
     if (items > INT_MAX) return cudaErrorInvalidValue;
     p.num_items = (int)items;
     if (reinterpret_cast<uintptr_t>(a.o_part) & 15u) return cudaErrorMisalignedAddress;
-    return launch<MODE_BLOCK>(p, a.q, a.M, a.k, a.v, a.Nctx, dev, s);
+    return launch<MODE_BLOCK, false>(p, a.q, a.M, a.k, a.v, a.Nctx, dev, s);
 }
 
 }  // namespace sattn
